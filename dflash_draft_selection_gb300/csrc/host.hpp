@@ -1,0 +1,66 @@
+// host.hpp -- host-side helpers of the DFlash 2 library: argument checks,
+// device attributes and per-kernel occupancy, cached per device.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "dflash2.h"
+
+namespace dfl {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int current_device() {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    return dev;
+}
+
+inline int sm_count() {
+    static int cache[64] = {0};
+    const int dev = current_device();
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+    if (dev >= 0 && dev < 64) cache[dev] = n;
+    return n;
+}
+
+// Resident CTAs per SM of `func` with the given block and dynamic shared
+// memory, after raising the kernel's dynamic shared-memory limit.  Cached per
+// (kernel, device).
+inline int blocks_per_sm(const void *func, int threads, size_t smem) {
+    struct Entry {
+        const void *f;
+        int dev;
+        int n;
+    };
+    static Entry cache[256];
+    static int used = 0;
+    static std::mutex mu;
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].f == func && cache[i].dev == dev) return cache[i].n;
+    if (smem > 48 * 1024)
+        cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess || n < 1)
+        n = 1;
+    if (used < 256) cache[used++] = Entry{func, dev, n};
+    return n;
+}
+
+inline dflash2_status after_launch() {
+    return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
+}
+
+inline int esize(dflash2_dtype dt) { return dt == DFLASH2_BF16 ? 2 : 4; }
+
+inline bool dtype_ok(dflash2_dtype dt) { return dt == DFLASH2_BF16 || dt == DFLASH2_F32; }
+
+}  // namespace dfl

@@ -1,0 +1,408 @@
+// verify.cu -- dflash2_verify: speculative-sampling verify of the proposed
+// path against the target logits.
+//
+// FreeToken PR 857, "Details"/Sampled verify: accept a drafted token with
+// probability min(1, p/q); on a reject resample from max(0, p - q), so the
+// output follows the target distribution; all-greedy batches keep the prefix
+// match.  DFlash 2 proposer issue, "Proposal" phase 3 (greedy stays
+// longest-prefix; rejection sampling restores the exact target distribution).
+// FreeToken PR 857, "Tests added or changed" (trusted, NaN, wrong-total and
+// greedy rows) fixes the per-request error rows.
+//
+// One launch: persistent CTAs scan the B*(K+1) target rows (argmax for greedy
+// requests, the filtered top-k distribution p for sampled ones) and publish a
+// small record per row in the workspace; a per-request ticket lets the CTA
+// that completes a request's last row run that request's accept walk.
+#include "filter.cuh"
+#include "host.hpp"
+#include "rowscan.cuh"
+
+namespace dfl {
+
+static __device__ unsigned int g_err_verify;
+
+struct TRec {
+    int32_t n;       // support size of p (1 for greedy rows)
+    int32_t flags;   // DFLASH2_ST_* of the row
+    int32_t ids[DFLASH2_MAX_TOPK];
+    float p[DFLASH2_MAX_TOPK];
+};
+
+struct VerifyArgs {
+    const int32_t *path_tok;
+    const int32_t *cand_idx;
+    const float *q_sel;
+    const int32_t *path_slot;
+    const float *u_acc;
+    const float *u_res;
+    uint32_t flags;
+    int32_t *accept_len;
+    int32_t *out_tok;
+    int32_t *status;
+    int32_t *tickets;
+    TRec *recs;
+    int K;
+};
+
+constexpr size_t TICKET_BYTES_ALIGN = 256;
+
+// ---------------------------------------------------------------- records --
+template <int R>
+__device__ void finalize_target(const RowResult<R> &res, const RowTask &task, TRec *rec, int lane) {
+    int32_t flags = DFLASH2_ST_OK;
+    if (task.mode == MODE_ARGMAX) {
+        const bool bad = res.bad || res.best == 0 || !isfinite(key_val(res.best));
+        if (bad) flags = DFLASH2_ST_NAN;
+        if (lane == 0) {
+            rec->n = bad ? 0 : 1;
+            rec->ids[0] = bad ? -1 : key_idx(res.best);
+            rec->p[0] = 1.0f;
+        }
+    } else {
+        const float z0 = key_val(res.list.k[0]);
+        const float z0b = __shfl_sync(FULL, z0, 0);
+        if (res.bad || !isfinite(z0b)) {
+            flags = DFLASH2_ST_NAN;
+            if (lane == 0) rec->n = 0;
+        } else {
+            float e[R], ek;
+            const int kept = topn_filter<R>(res.list, task, z0b, lane, e, &ek);
+            const float inv = 1.0f / ek;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int p = r * 32 + lane;
+                if (p < kept) {
+                    rec->ids[p] = key_idx(res.list.k[r]);
+                    rec->p[p] = e[r] * inv;
+                }
+            }
+            if (lane == 0) rec->n = kept;
+        }
+    }
+    if (lane == 0) rec->flags = flags;
+}
+
+// ------------------------------------------------------------ accept walk --
+struct DrawScratch {
+    int32_t ids[DFLASH2_MAX_TOPK];
+    float w[DFLASH2_MAX_TOPK];
+    int32_t sid[DFLASH2_MAX_TOPK];
+    float sw[DFLASH2_MAX_TOPK];
+};
+
+// Inverse CDF over the entries sorted by ascending token id: the first entry
+// whose running weight exceeds u * (total weight); if rounding leaves none,
+// the last entry with a positive weight.  Entries i < n are (id_i, w_i) with
+// i = r*32 + lane; ids are distinct.  Warp-uniform; returns the token.
+__device__ int32_t draw_ascending(const int32_t (&id)[2], const float (&w)[2], int n, float u,
+                                  DrawScratch &sc, int lane) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int i = r * 32 + lane;
+        if (i < n) {
+            sc.ids[i] = id[r];
+            sc.w[i] = w[r];
+        }
+    }
+    __syncwarp();
+    int rank[2] = {0, 0};
+    for (int j = 0; j < n; ++j) {
+        const int32_t idj = sc.ids[j];
+        rank[0] += idj < id[0];
+        rank[1] += idj < id[1];
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int i = r * 32 + lane;
+        if (i < n) {
+            sc.sid[rank[r]] = id[r];
+            sc.sw[rank[r]] = w[r];
+        }
+    }
+    __syncwarp();
+    int32_t pick = -1;
+    if (lane == 0) {
+        float Z = 0.0f;
+        for (int i = 0; i < n; ++i) Z += sc.sw[i];
+        const float thr = u * Z;
+        float cum = 0.0f;
+        int32_t last = -1;
+        for (int i = 0; i < n; ++i) {
+            const float wi = sc.sw[i];
+            if (wi <= 0.0f) continue;
+            cum += wi;
+            last = sc.sid[i];
+            if (pick < 0 && cum > thr) pick = sc.sid[i];
+        }
+        if (pick < 0) pick = last;
+    }
+    __syncwarp();
+    return __shfl_sync(FULL, pick, 0);
+}
+
+__device__ __forceinline__ int32_t ldcg_i(const int32_t *p) { return __ldcg(p); }
+__device__ __forceinline__ float ldcg_f(const float *p) { return __ldcg(p); }
+
+// The accept walk of request b (consumer warp 0 of the CTA that completed the
+// request's rows).
+__device__ void accept_request(const VerifyArgs &a, const dflash2_sampling *params, int64_t b,
+                               int64_t V, DrawScratch &sc, int lane) {
+    const int K = a.K;
+    const RowTask rt = decode_row(params, b, V, true);
+    const bool greedy = rt.mode == MODE_ARGMAX;
+    const TRec *rec = a.recs + b * (K + 1);
+    int st = DFLASH2_ST_OK;
+    if (rt.mode == MODE_SKIP) {
+        st = rt.status;
+    } else {
+        for (int t = 0; t <= K; ++t)
+            if (ldcg_i(&rec[t].flags) != DFLASH2_ST_OK) {
+                st = DFLASH2_ST_NAN;
+                break;
+            }
+    }
+    if (st == DFLASH2_ST_OK && !greedy) {
+        for (int t = 0; t < K; ++t) {
+            const int64_t o = (b * K + t) * NC;
+            const float qv = lane < NC ? a.q_sel[o + lane] : 0.0f;
+            if (__any_sync(FULL, lane < NC && (!isfinite(qv) || qv < 0.0f))) {
+                st = DFLASH2_ST_NAN;
+                break;
+            }
+            const float s = warp_sum(qv);
+            if (!(a.flags & DFLASH2_VERIFY_TRUST_Q) && fabsf(s - 1.0f) > 1e-3f) {
+                st = DFLASH2_ST_BAD_Q;
+                break;
+            }
+            const int js = a.path_slot[b * K + t];
+            if (js < 0 || js >= NC || a.cand_idx[o + js] != a.path_tok[b * K + t]) {
+                st = DFLASH2_ST_BAD_Q;
+                break;
+            }
+        }
+    }
+    int n = 0;
+    int32_t emit = -1;
+    if (st == DFLASH2_ST_OK) {
+        bool stopped = false;
+        for (int t = 0; t < K && !stopped; ++t) {
+            const int32_t d = a.path_tok[b * K + t];
+            if (greedy) {
+                const int32_t g = ldcg_i(&rec[t].ids[0]);
+                if (d == g) {
+                    ++n;
+                } else {
+                    emit = g;
+                    stopped = true;
+                }
+                continue;
+            }
+            const int rn = ldcg_i(&rec[t].n);
+            int32_t id[2];
+            float p[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int i = r * 32 + lane;
+                id[r] = i < rn ? ldcg_i(&rec[t].ids[i]) : -1;
+                p[r] = i < rn ? ldcg_f(&rec[t].p[i]) : 0.0f;
+            }
+            const float pd = warp_sum((id[0] == d && d >= 0 ? p[0] : 0.0f) +
+                                      (id[1] == d && d >= 0 ? p[1] : 0.0f));
+            const int64_t o = (b * K + t) * NC;
+            const float qd = a.q_sel[o + a.path_slot[b * K + t]];
+            if (a.u_acc[b * K + t] * qd < pd) {
+                ++n;
+                continue;
+            }
+            // residual max(0, p - q) over the support of p
+            const float qc = lane < NC ? a.q_sel[o + lane] : 0.0f;
+            const int32_t cc = lane < NC ? a.cand_idx[o + lane] : -1;
+            float r_[2] = {0.0f, 0.0f};
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                float qv = 0.0f;
+                for (int j = 0; j < NC; ++j) {
+                    const int32_t cj = __shfl_sync(FULL, cc, j);
+                    const float qj = __shfl_sync(FULL, qc, j);
+                    if (cj == id[r]) qv = qj;
+                }
+                const float diff = p[r] - qv;
+                r_[r] = (r * 32 + lane < rn && diff > 0.0f) ? diff : 0.0f;
+            }
+            const float Z = warp_sum(r_[0] + r_[1]);
+            const float u = a.u_res[b * (K + 1) + t];
+            if (Z > 1e-12f)
+                emit = draw_ascending(id, r_, rn, u, sc, lane);
+            else
+                emit = draw_ascending(id, p, rn, u, sc, lane);
+            stopped = true;
+        }
+        if (!stopped) {
+            if (greedy) {
+                emit = ldcg_i(&rec[K].ids[0]);
+            } else {
+                const int rn = ldcg_i(&rec[K].n);
+                int32_t id[2];
+                float p[2];
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int i = r * 32 + lane;
+                    id[r] = i < rn ? ldcg_i(&rec[K].ids[i]) : -1;
+                    p[r] = i < rn ? ldcg_f(&rec[K].p[i]) : 0.0f;
+                }
+                emit = draw_ascending(id, p, rn, a.u_res[b * (K + 1) + K], sc, lane);
+            }
+        }
+    }
+    for (int i = lane; i <= K; i += 32) {
+        int32_t v = -1;
+        if (st == DFLASH2_ST_OK) v = i < n ? a.path_tok[b * K + i] : (i == n ? emit : -1);
+        a.out_tok[b * (K + 1) + i] = v;
+    }
+    if (lane == 0) {
+        a.accept_len[b] = st == DFLASH2_ST_OK ? n : 0;
+        a.status[b] = st;
+    }
+}
+
+// Publish the row's record and, if it was the request's last row, run the
+// accept walk.  Consumer warp 0.
+__device__ void row_done(const VerifyArgs &a, const dflash2_sampling *params, int64_t row,
+                         int64_t V, DrawScratch &sc, int lane) {
+    const int64_t b = row / (a.K + 1);
+    __threadfence();
+    __syncwarp();
+    int old = 0;
+    if (lane == 0) old = atomicAdd(&a.tickets[b], 1);
+    old = __shfl_sync(FULL, old, 0);
+    if (old == a.K) {
+        if (lane == 0) a.tickets[b] = 0;
+        __threadfence();
+        accept_request(a, params, b, V, sc, lane);
+    }
+}
+
+template <int R, bool BF16>
+__global__ void __launch_bounds__(SCAN_THREADS) k_verify(ScanGeom g, VerifyArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *base = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
+    ScanSmem &sm = *reinterpret_cast<ScanSmem *>(base);
+    DrawScratch &sc = *reinterpret_cast<DrawScratch *>(base + sizeof(ScanSmem));
+    scan_init(sm);
+    if (threadIdx.x < 32) {
+        scan_producer<BF16>(sm, g, &g_err_verify);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    const int cw = (threadIdx.x >> 5) - 1;
+    uint32_t it = 0;
+    int rp = 0;
+    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x) {
+        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
+        TRec *rec = a.recs + row;
+        if (!row_streams(task)) {
+            if (cw == 0) {
+                if (lane == 0) {
+                    rec->n = 0;
+                    rec->flags = task.status;
+                }
+                row_done(a, g.params, row, g.V, sc, lane);
+            }
+            continue;
+        }
+        RowResult<R> res;
+        if (task.mode == MODE_ARGMAX)
+            scan_row<R, MODE_ARGMAX, BF16>(sm, g, task, row, it, rp, res, &g_err_verify);
+        else
+            scan_row<R, MODE_TOPN, BF16>(sm, g, task, row, it, rp, res, &g_err_verify);
+        if (cw == 0) {
+            finalize_target<R>(res, task, rec, lane);
+            row_done(a, g.params, row, g.V, sc, lane);
+        }
+        rp ^= 1;
+    }
+}
+
+template <int R, bool BF16>
+static dflash2_status launch_verify(const ScanGeom &g, const VerifyArgs &a, cudaStream_t stream) {
+    const size_t smem = sizeof(ScanSmem) + sizeof(DrawScratch) + 128;
+    const void *fn = reinterpret_cast<const void *>(&k_verify<R, BF16>);
+    const int per_sm = blocks_per_sm(fn, SCAN_THREADS, smem);
+    int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
+    if (grid > g.rows) grid = g.rows;
+    k_verify<R, BF16><<<static_cast<unsigned>(grid), SCAN_THREADS, smem, stream>>>(g, a);
+    return after_launch();
+}
+
+unsigned int read_error_verify(bool clear) {
+    unsigned int v = 0;
+    cudaMemcpyFromSymbol(&v, g_err_verify, sizeof v);
+    if (clear) {
+        const unsigned int z = 0;
+        cudaMemcpyToSymbol(g_err_verify, &z, sizeof z);
+    }
+    return v;
+}
+
+static size_t ticket_bytes(int64_t B) {
+    return (static_cast<size_t>(B) * sizeof(int32_t) + TICKET_BYTES_ALIGN - 1) / TICKET_BYTES_ALIGN *
+           TICKET_BYTES_ALIGN;
+}
+
+}  // namespace dfl
+
+using namespace dfl;
+
+extern "C" size_t dflash2_verify_workspace_bytes(int64_t B, int32_t K) {
+    if (B < 0 || K < 1 || K > DFLASH2_MAX_K) return 0;
+    return ticket_bytes(B) + static_cast<size_t>(B) * (K + 1) * sizeof(TRec);
+}
+
+extern "C" dflash2_status dflash2_verify(const void *tlogits, dflash2_dtype dt, int64_t B, int32_t K,
+                                         int64_t V, int64_t ld, const int32_t *path_tok,
+                                         const int32_t *cand_idx, const float *q_sel,
+                                         const int32_t *path_slot, const dflash2_sampling *params,
+                                         const float *u_acc, const float *u_res, uint32_t flags,
+                                         int32_t *accept_len, int32_t *out_tok, int32_t *status,
+                                         void *ws, size_t ws_bytes, dflash2_stream stream) {
+    if (!dtype_ok(dt) || B < 0 || K < 1 || K > DFLASH2_MAX_K || V < NC || V >= (int64_t(1) << 31) ||
+        ld < V)
+        return DFLASH2_ERR_INVALID_ARG;
+    const int es = esize(dt);
+    if ((ld * es) % 16 != 0) return DFLASH2_ERR_INVALID_ARG;
+    if (B == 0) return DFLASH2_OK;
+    if (!tlogits || !aligned16(tlogits) || !path_tok || !cand_idx || !q_sel || !path_slot ||
+        !accept_len || !out_tok || !status || !ws)
+        return DFLASH2_ERR_INVALID_ARG;
+    if (params && (!u_acc || !u_res)) return DFLASH2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return DFLASH2_ERR_INVALID_ARG;
+    if (ws_bytes < dflash2_verify_workspace_bytes(B, K)) return DFLASH2_ERR_WORKSPACE;
+    ScanGeom g;
+    g.base = static_cast<const char *>(tlogits);
+    g.ld_bytes = ld * es;
+    g.V = V;
+    g.rows = B * (K + 1);
+    g.tiles_per_row = static_cast<int>((V * es + TILE_BYTES - 1) / TILE_BYTES);
+    g.params = params;
+    g.rows_per_param = K + 1;
+    g.target = true;
+    VerifyArgs a;
+    a.path_tok = path_tok;
+    a.cand_idx = cand_idx;
+    a.q_sel = q_sel;
+    a.path_slot = path_slot;
+    a.u_acc = u_acc;
+    a.u_res = u_res;
+    a.flags = flags;
+    a.accept_len = accept_len;
+    a.out_tok = out_tok;
+    a.status = status;
+    a.tickets = static_cast<int32_t *>(ws);
+    a.recs = reinterpret_cast<TRec *>(static_cast<char *>(ws) + ticket_bytes(B));
+    a.K = K;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (params == nullptr)
+        return dt == DFLASH2_BF16 ? launch_verify<1, true>(g, a, s) : launch_verify<1, false>(g, a, s);
+    return dt == DFLASH2_BF16 ? launch_verify<2, true>(g, a, s) : launch_verify<2, false>(g, a, s);
+}

@@ -1,0 +1,226 @@
+/*
+ * dflash2.h -- C ABI of the DFlash 2 draft-selection + verify path on one GPU.
+ *
+ * The DFlash 2 proposer keeps the 16 best candidates of every drafted
+ * position, scores adjacent candidate pairs with a low-rank bilinear term
+ * gated by the drafter's hidden state, walks those scores once to pick the
+ * proposed path, and the verify accepts drafted tokens with probability
+ * min(1, p/q) and resamples a rejected one from max(0, p - q).  Sources:
+ *   [P] "qwen3/dflash: DFlash 2 proposer -- top-16 path selector + two-tap
+ *       dynamic convolution" (pegainfer issue 930): "What upstream shipped"
+ *       items 1-2, "Proposal" phases 1-3.
+ *   [F] FreeToken PR 857 (DFlash 2 next to MTP): "Details" (Runtime, Sampled
+ *       verify, Refused at startup), "Tests added or changed", "Known gaps".
+ *
+ * Conventions shared by every entry point
+ *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
+ *     16-byte aligned.  Nothing here allocates, frees or synchronises: each
+ *     call enqueues its kernels on `stream` and returns.
+ *   - A call returns DFLASH2_ERR_INVALID_ARG before launching anything when an
+ *     argument is out of range (see each call); DFLASH2_ERR_CUDA when a launch
+ *     fails (the CUDA error is left for cudaGetLastError).
+ *   - Per-request data problems never abort a batch: they are reported per
+ *     request in `status` (DFLASH2_ST_*) or as -1 / NaN outputs.
+ *   - Workspaces (`ws`) are caller-provided device buffers of at least the
+ *     size returned by the matching *_workspace_bytes function.  They must be
+ *     zero-filled once before first use; every call leaves them zeroed again.
+ *     Two calls that share a workspace must not run concurrently.
+ *   - The first call on a device performs one-time set-up (device attributes,
+ *     kernel attributes); make it before any stream capture.  Later calls are
+ *     capturable into CUDA graphs.
+ *   - Ties in logits are broken by the lower token id everywhere.
+ */
+#ifndef DFLASH2_H
+#define DFLASH2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *dflash2_stream;
+
+typedef enum {
+    DFLASH2_OK = 0,
+    DFLASH2_ERR_INVALID_ARG = 1,
+    DFLASH2_ERR_UNSUPPORTED = 2,
+    DFLASH2_ERR_CUDA = 3,
+    DFLASH2_ERR_WORKSPACE = 4
+} dflash2_status;
+
+typedef enum { DFLASH2_F32 = 0, DFLASH2_BF16 = 1 } dflash2_dtype;
+
+/* Per-request verify status. */
+enum {
+    DFLASH2_ST_OK = 0,
+    DFLASH2_ST_NAN = 1,         /* NaN or +Inf (or no value above -Inf) in a target row; NaN, Inf or
+                                   a negative value in a q row */
+    DFLASH2_ST_BAD_Q = 2,       /* a q row does not sum to 1 within 1e-3, or a drafted token is not
+                                   the candidate at its slot */
+    DFLASH2_ST_BAD_PARAMS = 3,  /* temperature < 0 or not finite, top_k < 0, top_p outside (0, 1] */
+    DFLASH2_ST_UNSUPPORTED = 4  /* see dflash2_sampling */
+};
+
+#define DFLASH2_NC 16        /* candidates per draft position ([P] item 1) */
+#define DFLASH2_MAX_K 15     /* drafted positions: 1 .. block_size - 1 with block_size <= 16 ([F] Refused at startup) */
+#define DFLASH2_MAX_TOPK 64  /* largest top_k a filtered row may use */
+
+/*
+ * Sampling parameters of one request, applied to draft and target alike in
+ * the order temperature -> top_k -> renormalise -> top_p -> renormalise
+ * ([F] "Speed": temperature 1.0, top_p 0.95, top_k 20 on both sides).
+ * temperature == 0 is greedy.  top_k == 0 (or >= V) and top_p == 1 switch the
+ * filters off.  This build supports, for temperature > 0: any top_p with
+ * 1 <= effective top_k <= 64, and no filter at all on the draft side; an
+ * unfiltered sampled target row, or a filtered row with top_k == 0 or
+ * top_k > 64, is DFLASH2_ST_UNSUPPORTED.
+ */
+typedef struct {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+} dflash2_sampling;
+
+/*
+ * dflash2_topk16 -- [P] item 1 "keep top-16 candidates per position"; [F]
+ * Runtime "the target LM head gives 16 candidates per slot".
+ *
+ * logits   [rows, ld] of dt (row stride ld elements, ld >= V, ld * elem
+ *          size a multiple of 16 bytes); the first V entries of a row count.
+ * params   device [ceil(rows / rows_per_param)] or NULL (all greedy); row r
+ *          uses params[r / rows_per_param].
+ * cand_idx [rows, 16] int32: the 16 best tokens, best first.
+ * cand_U   [rows, 16] f32: log-probability of each candidate under the
+ *          drafter's distribution: greedy rows log softmax(z), sampled rows
+ *          log of the filtered softmax(z / T), -inf for a candidate the
+ *          filter drops.
+ * lse      [rows] f32: the log normaliser on the z / T' scale (T' = 1 for
+ *          greedy rows), so that kept candidates have U = z / T' - lse.
+ * A row holding a NaN or +Inf, or nothing above -Inf, or with invalid or
+ * unsupported parameters, gets cand_idx -1, U NaN and lse NaN.
+ * Errors: INVALID_ARG if a pointer is NULL or misaligned, rows < 0, V < 16,
+ * V >= 2^31, ld < V, ld * elem size not a multiple of 16, rows_per_param < 1.
+ */
+dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
+                              int64_t ld, const dflash2_sampling *params, int64_t rows_per_param,
+                              int32_t *cand_idx, float *cand_U, float *lse, dflash2_stream stream);
+
+/*
+ * dflash2_ctx_gate -- [P] item 1 "context gate" of the bilinear selector,
+ * taken as gate = sigmoid(W_g h) with no bias.
+ *
+ * h     [n, hidden] of dt;  Wg [D, hidden] of dt;  gate [n, D] f32.
+ * bf16 runs on the tensor cores (fp32 accumulation); f32 on the CUDA cores.
+ * Errors: INVALID_ARG if a pointer is NULL or misaligned, n < 0, D not in
+ * {16, 32, ..., 512} (a power of two), hidden < 1, or (bf16) hidden not a
+ * multiple of 64.
+ */
+dflash2_status dflash2_ctx_gate(const void *h, dflash2_dtype dt, int64_t n, int64_t hidden,
+                                const void *Wg, int32_t D, float *gate, dflash2_stream stream);
+
+/*
+ * dflash2_pair_score_walk -- [P] item 1 (S_t(a,b) = U_t(b) + <A(a) * H(h_t),
+ * B(b)>, one greedy or sampled walk over the precomputed scores) and
+ * "Proposal" phase 1 (block_size x 16 preds x 16 cands x 256 dims, a
+ * <= block_size-step argmax walk); [F] Runtime (sampled from q, argmax when
+ * greedy).
+ *
+ * cand_idx [B, K, 16] int32, cand_U [B, K, 16] f32 (from dflash2_topk16).
+ * last_tok [B] int32: the last verified token, the only predecessor at t = 0.
+ * A, Bt    [V, D] of tdt: the two token-embedding tables.
+ * gate     [B, K, D] f32 (from dflash2_ctx_gate).
+ * params   [B] or NULL (all greedy); only temperature is read (0 = greedy).
+ * u_walk   [B, K] f32 uniforms in [0, 1); may be NULL when params is NULL.
+ * Outputs: path_tok [B, K] int32, path_slot [B, K] int32 (index into the
+ *   candidates), q_sel [B, K, 16] f32 (the walk's distribution at each step;
+ *   one-hot when greedy), scores [B, K, 16, 16] f32: scores[b,t,i,j] pairs
+ *   predecessor i with candidate j; at t = 0 row 0 is the last verified
+ *   token and rows 1..15 are -inf.
+ * Greedy steps take the first slot with the largest score; sampled steps
+ * take the first slot whose cumulative q exceeds u_walk.  A step whose row
+ * holds a NaN, or only -inf, ends the walk: that step and the rest get
+ * token -1, slot -1 and NaN q.  Ids outside [0, V) give NaN scores.
+ * ws: dflash2_pair_score_walk_workspace_bytes(B).
+ * Errors: INVALID_ARG for NULL/misaligned pointers, B < 0, K outside 1..15,
+ * D not a power of two in 16..1024, V < 16, u_walk NULL with params set.
+ */
+size_t dflash2_pair_score_walk_workspace_bytes(int64_t B);
+dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand_idx,
+                                       const float *cand_U, const int32_t *last_tok,
+                                       const void *A, const void *Bt, dflash2_dtype tdt, int64_t V,
+                                       int32_t D, const float *gate,
+                                       const dflash2_sampling *params, const float *u_walk,
+                                       int32_t *path_tok, int32_t *path_slot, float *q_sel,
+                                       float *scores, void *ws, size_t ws_bytes,
+                                       dflash2_stream stream);
+
+/*
+ * dflash2_verify -- [F] Sampled verify (accept with min(1, p/q); on a reject
+ * resample from max(0, p - q); all-greedy batches keep the prefix match);
+ * [P] "Proposal" phase 3; [F] "Tests added or changed" (trusted, NaN,
+ * wrong-total and greedy rows).
+ *
+ * tlogits [B, K+1, ld] of dt: target logits of the K drafted positions and
+ *   the bonus position, row (b, t) at (b * (K+1) + t) * ld.
+ * path_tok, path_slot [B, K]; cand_idx, q_sel [B, K, 16] (from the walk).
+ * params [B] or NULL (all greedy).  u_acc [B, K], u_res [B, K+1] f32
+ *   uniforms in [0, 1); may be NULL when params is NULL.
+ * flags: DFLASH2_VERIFY_TRUST_Q skips the q-total check.
+ * Per request b: p_t is the target distribution of row t (greedy: all mass
+ *   on the argmax).  Greedy requests accept while the drafted token is the
+ *   argmax and then emit the argmax.  Sampled requests accept position t iff
+ *   u_acc[t] * q < p at the drafted token; on a reject they draw from
+ *   max(0, p - q) (normalised; from p when its total is <= 1e-12) by inverse
+ *   CDF over ascending token ids with u_res[t]; after K accepts they draw the
+ *   bonus token from p_K with u_res[K].
+ * Outputs: accept_len [B] in 0..K; out_tok [B, K+1]: the accepted tokens,
+ *   then the corrected or bonus token, then -1; status [B] (DFLASH2_ST_*).
+ *   A request with status != 0 commits nothing (accept_len 0, all -1).
+ * ws: dflash2_verify_workspace_bytes(B, K).
+ * Errors: INVALID_ARG as for dflash2_topk16 plus K outside 1..15 and NULL
+ * uniforms with params set.
+ */
+#define DFLASH2_VERIFY_TRUST_Q 1u
+size_t dflash2_verify_workspace_bytes(int64_t B, int32_t K);
+dflash2_status dflash2_verify(const void *tlogits, dflash2_dtype dt, int64_t B, int32_t K,
+                              int64_t V, int64_t ld, const int32_t *path_tok,
+                              const int32_t *cand_idx, const float *q_sel,
+                              const int32_t *path_slot, const dflash2_sampling *params,
+                              const float *u_acc, const float *u_res, uint32_t flags,
+                              int32_t *accept_len, int32_t *out_tok, int32_t *status, void *ws,
+                              size_t ws_bytes, dflash2_stream stream);
+
+/*
+ * dflash2_conv2tap -- [P] item 2: Conv(x)_t = k_{t,0} * x_t + k_{t,1} * x_{t-1},
+ * the first position tapping the last verified token's hidden state; [F]
+ * Refused at startup (conv_group_size divides the hidden size).
+ *
+ * x [B, T, H], k0 and k1 [B, T, H / group_size], x_prev [B, H], y [B, T, H],
+ * all of dt.  With group_size G, channel c uses tap c / G.  bf16 outputs are
+ * the exact value rounded once to bf16 (nearest, ties to even); f32 outputs
+ * use one fused multiply-add.
+ * Errors: INVALID_ARG for NULL/misaligned pointers, B < 0, T < 1, H < 1,
+ * group_size < 1 or not dividing H.
+ */
+dflash2_status dflash2_conv2tap(const void *x, const void *k0, const void *k1, const void *x_prev,
+                                dflash2_dtype dt, int64_t B, int32_t T, int64_t H,
+                                int32_t group_size, void *y, dflash2_stream stream);
+
+/* Human-readable name of a status code (static string). */
+const char *dflash2_status_string(dflash2_status s);
+
+/*
+ * Error word of the library's kernels on the current device: nonzero after a
+ * kernel gave up on a bounded wait (it then wrote -1 / NaN outputs instead of
+ * hanging).  Synchronises the device.  clear != 0 resets the word.
+ */
+dflash2_status dflash2_device_error(uint32_t *code, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH2_H */

@@ -1,0 +1,149 @@
+"""dflash2_topk16 against the oracle (bit-exact ids, U and lse within 1e-4 rel)."""
+import numpy as np
+import pytest
+import torch
+
+import dflash_draft_selection_gb300 as d2
+from dflash_draft_selection_gb300 import synth
+from tests._util import MARGIN, assert_close, cuda_or_skip, params_np
+
+pytestmark = pytest.mark.gpu
+
+
+def run_both(ref, z, params=None, rpp=1, V=None):
+    dev = cuda_or_skip()
+    zg = z.to(dev)
+    pg = None if params is None else d2.sampling_params(params["temperature"], params["top_k"], params["top_p"],
+                                                        device=dev)
+    Vv = z.shape[1] if V is None else V
+    idx, U, lse = d2.topk16(zg, params=pg, rows_per_param=rpp, V=Vv)
+    torch.cuda.synchronize()
+    r_idx, r_U, r_lse, r_mg = ref.topk16(z, params=params, rows_per_param=rpp, V=Vv, ld=z.shape[1])
+    return idx.cpu().numpy(), U.cpu().numpy(), lse.cpu().numpy(), r_idx, r_U, r_lse, r_mg
+
+
+def compare(res, what):
+    idx, U, lse, r_idx, r_U, r_lse, r_mg = res
+    np.testing.assert_array_equal(idx, r_idx, err_msg=what)
+    ok = r_mg >= MARGIN  # rows whose top_p decision is within rounding of the threshold are exempt
+    assert_close(U[ok], r_U[ok], what=what + " U")
+    assert_close(lse[ok], r_lse[ok], what=what + " lse")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("V", [16, 17, 100, 4096, 8192 + 13, 40000])
+def test_greedy_random(ref, dtype, V):
+    g = torch.Generator().manual_seed(V)
+    z = (torch.randn(11, V, generator=g) * 3).to(dtype)
+    compare(run_both(ref, z), f"greedy V={V} {dtype}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_ties_zero_signs_and_duplicates(ref, dtype):
+    V = 9000
+    g = torch.Generator().manual_seed(1)
+    z = (torch.randint(-4, 4, (8, V), generator=g).float() * 0.25).to(dtype)
+    z[1] = 2.0                           # all equal
+    z[2, ::2] = -0.0
+    z[2, 1::2] = 0.0
+    z[3, [5, 8000, 20]] = 7.0            # triple maximum
+    compare(run_both(ref, z), "ties")
+
+
+def test_padded_rows_ld_greater_than_V(ref):
+    V, ld = 5000, 5008
+    z = torch.randn(6, ld).bfloat16()
+    z[:, V:] = 100.0                     # padding must not be read
+    dev = cuda_or_skip()
+    idx, U, lse = d2.topk16(z.to(dev), V=V)
+    r_idx, r_U, r_lse, _ = ref.topk16(z, V=V, ld=ld)
+    np.testing.assert_array_equal(idx.cpu().numpy(), r_idx)
+    assert_close(U.cpu().numpy(), r_U)
+
+
+@pytest.mark.parametrize("T,k,p", [(0.0, 0, 1.0), (0.7, 0, 1.0), (1.0, 20, 0.95), (1.0, 64, 1.0),
+                                   (0.5, 5, 0.5), (2.0, 1, 1.0), (1.0, 16, 0.3), (1.3, 40, 0.99)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_sampled_filters(ref, T, k, p, dtype):
+    g = torch.Generator().manual_seed(int(T * 10) + k)
+    z = (torch.randn(12, 6000, generator=g) * 2.5).to(dtype)
+    compare(run_both(ref, z, params=params_np(12, T, k, p)), f"T={T} k={k} p={p}")
+
+
+def test_mixed_params_per_request(ref):
+    B, K, V = 4, 3, 3000
+    z = (torch.randn(B * K, V) * 2).bfloat16()
+    p = params_np(B, 1.0, 20, 0.95)
+    p["temperature"][1] = 0.0
+    p["top_k"][2] = 0
+    p["top_p"][2] = 1.0
+    p["temperature"][3] = 0.5
+    compare(run_both(ref, z, params=p, rpp=K), "mixed")
+
+
+def test_bad_rows_and_params(ref):
+    V = 700
+    z = torch.randn(6, V)
+    z[0, 5] = float("nan")
+    z[1, 9] = float("inf")
+    z[2, :] = float("-inf")
+    z[3, :690] = float("-inf")
+    idx, U, lse, r_idx, r_U, r_lse, _ = run_both(ref, z)
+    np.testing.assert_array_equal(idx, r_idx)
+    assert_close(U, r_U)
+    p = params_np(6, 1.0, 10, 1.0)
+    p["top_p"][4] = 0.0                  # invalid
+    p["temperature"][5] = -1.0           # invalid
+    idx, U, lse, r_idx, r_U, r_lse, _ = run_both(ref, z, params=p)
+    np.testing.assert_array_equal(idx, r_idx)
+    assert np.all(idx[4:] == -1) and np.all(np.isnan(U[4:]))
+
+
+def test_unsupported_params_flagged(ref):
+    dev = cuda_or_skip()
+    z = torch.randn(3, 500).to(dev)
+    for k, p in [(0, 0.9), (65, 1.0), (100, 0.5)]:
+        idx, U, lse = d2.topk16(z, params=d2.sampling_params([1.0] * 3, [k] * 3, [p] * 3, device=dev))
+        assert torch.all(idx == -1) and torch.all(torch.isnan(U))
+
+
+def test_empty_and_invalid(ref):
+    dev = cuda_or_skip()
+    z = torch.randn(0, 100, device=dev)
+    idx, U, lse = d2.topk16(z)
+    assert idx.shape == (0, 16)
+    with pytest.raises(d2.DFlash2Error):
+        d2.topk16(torch.randn(2, 8, device=dev))          # V < 16
+    with pytest.raises(d2.DFlash2Error):
+        d2.topk16(torch.randn(2, 100, device=dev).bfloat16()[:, :99], V=99)  # ld*2 not 16-aligned? (ld=100 ok)
+
+
+@pytest.mark.parametrize("name", ["27b_greedy", "27b_sampled", "stress"])
+def test_full_size_sampled_rows(ref, name):
+    """The full workload in the bench's launch configuration; a sample of rows checked one by one."""
+    dev = cuda_or_skip()
+    shp = synth.WORKLOADS[name]
+    g = torch.Generator(device=dev).manual_seed(shp.seed)
+    rows = shp.B * shp.K
+    z = synth.spike_logits(rows, shp.V, g, dev).to(shp.dtype)
+    if shp.dup_frac:
+        synth.duplicate_max(z, shp.dup_frac, g)
+    p = synth.make_params(shp.B, shp.temperature, shp.top_k, shp.top_p)
+    pg = d2.sampling_params(p["temperature"], p["top_k"], p["top_p"], device=dev)
+    idx, U, lse = d2.topk16(z, params=pg if shp.temperature > 0 else None, rows_per_param=shp.K)
+    torch.cuda.synchronize()
+    pick = torch.randperm(rows, generator=torch.Generator().manual_seed(0))[:24].sort().values
+    if shp.dup_frac:  # include rows with a duplicated maximum
+        zz = z.float()
+        mx = zz.max(dim=1, keepdim=True).values
+        dup = ((zz == mx).sum(dim=1) > 1).nonzero().flatten()[:8].cpu()
+        assert dup.numel() > 0
+        pick = torch.cat([pick, dup]).unique()
+    zs = z[pick.to(dev)].cpu()
+    pr = None if shp.temperature == 0 else np.repeat(p[:1], len(pick))
+    r_idx, r_U, r_lse, r_mg = ref.topk16(zs, params=pr)
+    np.testing.assert_array_equal(idx.cpu().numpy()[pick.numpy()], r_idx)
+    ok = r_mg >= MARGIN
+    assert_close(U.cpu().numpy()[pick.numpy()][ok], r_U[ok], what=name + " U")
+    assert_close(lse.cpu().numpy()[pick.numpy()][ok], r_lse[ok], what=name + " lse")
+    assert d2.device_error() == 0
