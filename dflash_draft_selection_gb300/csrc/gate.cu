@@ -95,7 +95,9 @@ __device__ __forceinline__ void tma_load_2d(void *sdst, const CUtensorMap *tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
 }
+// Aligned cluster barrier: reconverge the warp first.
 __device__ __forceinline__ void cluster_sync() {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -163,6 +165,7 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
         sm.issued = 0;
         fence_barrier_init();
     }
+    __syncwarp();
     if (warp == 1) tmem_alloc(&sm.tmem_base, TCOLS);
     tc_fence_before();
     __syncthreads();
@@ -190,7 +193,7 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
         for (int i = 0; i < nkb; ++i) {
             const int s = i % GSTAGES;
             const bool quick = *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
-            if (!mbar_wait(&sm.full[s], (i / GSTAGES) & 1, quick ? 0 : 2000000000ull)) {
+            if (!mbar_wait(&sm.full[s], (i / GSTAGES) & 1, quick ? 0 : 4000000000ll)) {
                 atomicOr(&g_err_gate, ERR_WAIT_TIMEOUT);
                 *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
                 break;
@@ -209,6 +212,7 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
 
     // Epilogue: tensor memory -> shared partial tile.
     const bool ok = mbar_wait(&sm.accum, 0) && *reinterpret_cast<volatile int *>(&sm.abort_flag) == 0;
+    __syncwarp();  // tcgen05.ld below is warp-aligned
     tc_fence_after();
     float *part = reinterpret_cast<float *>(&sm.a[0][0]);
     const int row = warp * 32 + lane;
@@ -256,10 +260,11 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
     if (threadIdx.x == 0) {
         const int issued = sm.issued;
         for (int i = issued > GSTAGES ? issued - GSTAGES : 0; i < issued; ++i)
-            mbar_wait(&sm.full[i % GSTAGES], (i / GSTAGES) & 1, 100000000ull);
+            mbar_wait(&sm.full[i % GSTAGES], (i / GSTAGES) & 1, 200000000ll);
     }
     __syncthreads();
     tc_fence_after();
+    __syncwarp();
     if (warp == 1) tmem_dealloc(tmem, TCOLS);
 }
 

@@ -3,53 +3,56 @@
 // Both logit streams of the DFlash 2 path (the drafter's block logits for the
 // top-16 candidates and U, the target's verify logits for p) are reductions
 // of whole vocabulary rows: a running max / sum of exponentials, an argmax,
-// or the best N keys.  A persistent CTA owns whole rows.  One producer warp
-// streams 8 KB tiles of the row into a shared-memory ring with 1-D bulk
-// copies (cp.async.bulk, completion on mbarriers); eight consumer warps read
-// the tiles once and keep, per thread, the running max and sum of
-// exponentials (or argmax), and, per warp, a register-resident list of the
-// best keys filtered by a CTA-wide threshold.  At the end of a row the warp
-// results are merged (bitonic networks) and consumer warp 0 holds the row
-// result.  Every wait is bounded: on time-out the CTA raises the error word,
-// stops waiting and flags the rows it could not read.
+// or the best N keys.  A persistent CTA of 8 warps owns whole rows.  Each
+// warp streams its own interleaved 2 KB chunks of the row (chunk c belongs to
+// warp c mod 8) through a private 4-stage shared-memory ring filled by 1-D
+// bulk copies (cp.async.bulk) that complete on per-stage mbarriers; the warp
+// that consumes a stage is the one that refills it, so no cross-warp
+// handshake is needed.  Each thread keeps the running max and sum of
+// exponentials (or argmax) of its elements, each warp a register-resident
+// list of its best keys filtered by a CTA-wide threshold.  At the end of a
+// row the warp results are merged (bitonic networks) and warp 0 holds the
+// row result.  Waits are bounded: a warp that times out raises the error
+// word, stops issuing copies, waits a bounded time for those in flight and
+// flags its rows.
 #pragma once
 
 #include "common.cuh"
 
 namespace dfl {
 
-constexpr int TILE_BYTES = 8192;
-constexpr int STAGES = 5;
-constexpr int CWARPS = 8;
-constexpr int CTHREADS = CWARPS * 32;
-constexpr int SCAN_THREADS = CTHREADS + 32;
-constexpr int VEC_PER_TILE = TILE_BYTES / 16;
-constexpr int VEC_PER_THREAD = VEC_PER_TILE / CTHREADS;
-constexpr int BAR_CONSUMERS = 1;  // named barrier id of the consumer warps
+constexpr int CHUNK_BYTES = 2048;
+constexpr int WSTAGES = 4;
+constexpr int SCAN_WARPS = 8;
+constexpr int SCAN_THREADS = SCAN_WARPS * 32;
+constexpr int VEC_PER_CHUNK = CHUNK_BYTES / 16;
+constexpr int VEC_PER_LANE = VEC_PER_CHUNK / 32;
+constexpr long long WAIT_CYCLES = 4000000000ll;  // ~2 s at 2 GHz
+constexpr long long DRAIN_CYCLES = 200000000ll;  // ~0.1 s
 
 struct ScanGeom {
     const char *base;  // logits
     int64_t ld_bytes;  // row stride in bytes
     int64_t V;
     int64_t rows;
-    int tiles_per_row;
+    int chunks_per_row;
     const dflash2_sampling *params;
     int64_t rows_per_param;
     bool target;
 };
 
 struct ScanSmem {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[SCAN_WARPS][WSTAGES];
     unsigned long long tau[2];
-    int abort_flag;
     int bad[2];
-    float wm[CWARPS];
-    float wsum[CWARPS];
-    uint64_t wbest[CWARPS];
-    uint64_t lists[CWARPS][64];
-    alignas(128) unsigned char tiles[STAGES][TILE_BYTES];
+    float wm[SCAN_WARPS];
+    float wsum[SCAN_WARPS];
+    uint64_t wbest[SCAN_WARPS];
+    uint64_t lists[SCAN_WARPS][64];
+    alignas(128) unsigned char buf[SCAN_WARPS][WSTAGES][CHUNK_BYTES];
 };
+
+constexpr size_t scan_smem_bytes() { return sizeof(ScanSmem) + 128; }
 
 template <int R>
 struct RowResult {
@@ -59,7 +62,61 @@ struct RowResult {
     bool bad;          // NaN seen or a wait failed
 };
 
-// Per-thread scan state for one row.
+// ------------------------------------------------------ per-warp streams ----
+// Item k of warp w is chunk w + 8 (k mod n_w) of the CTA's (k / n_w)-th row.
+struct WarpStream {
+    int w;          // warp index
+    int n_w;        // chunks per row owned by this warp
+    int64_t total;  // items over all rows of this CTA
+    int64_t issued;
+    int64_t consumed;
+    bool aborted;
+};
+
+__device__ __forceinline__ uint32_t chunk_bulk_bytes(const ScanGeom &g, int c, int esz) {
+    int64_t bytes = g.V * esz - static_cast<int64_t>(c) * CHUNK_BYTES;
+    if (bytes > CHUNK_BYTES) bytes = CHUNK_BYTES;
+    return static_cast<uint32_t>(bytes & ~static_cast<int64_t>(15));
+}
+
+// Lane 0 issues item k of the warp's stream into its stage.
+template <int ESZ>
+__device__ __forceinline__ void stream_issue(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, int64_t k,
+                                             int lane) {
+    const int stage = static_cast<int>(k % WSTAGES);
+    const int64_t row = blockIdx.x + (k / ws.n_w) * gridDim.x;
+    const int c = ws.w + SCAN_WARPS * static_cast<int>(k % ws.n_w);
+    if (lane == 0) {
+        const uint32_t bytes = chunk_bulk_bytes(g, c, ESZ);
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&sm.full[ws.w][stage], bytes);
+        if (bytes)
+            bulk_g2s(sm.buf[ws.w][stage], g.base + row * g.ld_bytes + static_cast<int64_t>(c) * CHUNK_BYTES,
+                     bytes, &sm.full[ws.w][stage]);
+    }
+    __syncwarp();
+}
+
+template <int ESZ>
+__device__ __forceinline__ void stream_start(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, int lane) {
+    ws.w = threadIdx.x >> 5;
+    ws.n_w = ws.w < g.chunks_per_row ? (g.chunks_per_row - ws.w + SCAN_WARPS - 1) / SCAN_WARPS : 0;
+    const int64_t my_rows = blockIdx.x < g.rows ? (g.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    ws.total = my_rows * ws.n_w;
+    ws.issued = 0;
+    ws.consumed = 0;
+    ws.aborted = false;
+    while (ws.issued < ws.total && ws.issued < WSTAGES) stream_issue<ESZ>(sm, g, ws, ws.issued++, lane);
+}
+
+// After a time-out: wait a bounded time for the copies still in flight.
+__device__ __forceinline__ void stream_drain(ScanSmem &sm, WarpStream &ws) {
+    for (int64_t k = ws.consumed; k < ws.issued; ++k)
+        mbar_wait(&sm.full[ws.w][k % WSTAGES], static_cast<uint32_t>((k / WSTAGES) & 1), DRAIN_CYCLES);
+    __syncwarp();
+}
+
+// ------------------------------------------------------------ scan state ----
 template <int R>
 struct ScanState {
     float bv;
@@ -220,58 +277,19 @@ struct VecLoad<false> {
 
 __device__ __forceinline__ bool row_streams(const RowTask &t) { return t.mode != MODE_SKIP; }
 
-// Bytes the bulk copy of tile j moves (the ragged < 16-byte end of a row is
-// read by the consumers straight from global memory).
-__device__ __forceinline__ uint32_t tile_bulk_bytes(const ScanGeom &g, int j, int esz) {
-    const int64_t te = TILE_BYTES / esz;
-    int64_t cnt = g.V - static_cast<int64_t>(j) * te;
-    if (cnt > te) cnt = te;
-    return static_cast<uint32_t>((cnt * esz) & ~static_cast<int64_t>(15));
-}
-
-// Producer warp: stream every tile of every row this CTA owns.
-template <bool BF16>
-__device__ void scan_producer(ScanSmem &sm, const ScanGeom &g, unsigned int *err_word) {
-    constexpr int esz = BF16 ? 2 : 4;
-    if ((threadIdx.x & 31) != 0) return;
-    uint32_t it = 0;
-    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x) {
-        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, g.target);
-        if (!row_streams(task)) continue;
-        const char *rbase = g.base + row * g.ld_bytes;
-        for (int j = 0; j < g.tiles_per_row; ++j, ++it) {
-            const int stage = it % STAGES;
-            if (it >= STAGES) {
-                const bool quick = *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
-                if (!mbar_wait(&sm.empty[stage], ((it / STAGES) & 1) ^ 1, quick ? 0 : 2000000000ull)) {
-                    atomicOr(err_word, ERR_WAIT_TIMEOUT);
-                    *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
-                }
-            }
-            const uint32_t bytes = tile_bulk_bytes(g, j, esz);
-            mbar_arrive_expect_tx(&sm.full[stage], bytes);
-            if (bytes) bulk_g2s(sm.tiles[stage], rbase + static_cast<int64_t>(j) * TILE_BYTES, bytes,
-                                &sm.full[stage]);
-        }
-    }
-    // Drain: do not leave copies in flight into this CTA's shared memory.
-    const uint32_t first = it > STAGES ? it - STAGES : 0;
-    for (uint32_t t = first; t < it; ++t) mbar_wait(&sm.full[t % STAGES], (t / STAGES) & 1, 100000000ull);
-}
-
-// Consumer warps: scan one row; on return consumer warp 0 holds the result.
-// `it` is the CTA's running tile counter, `rp` the parity of this row among
-// the rows the CTA scanned.
+// Consume the warp's chunks of one row of the CTA (global row `row`) and
+// merge the warps; on return warp 0 holds the result.  Every row of the CTA
+// goes through here (rows that need no scan with `skip`), so that the chunk
+// streams stay in step.  `rp` is the parity of this row among the CTA's rows.
 template <int R, int MODE, bool BF16>
-__device__ void scan_row(ScanSmem &sm, const ScanGeom &g, const RowTask &task, int64_t row,
-                         uint32_t &it, int rp, RowResult<R> &res, unsigned int *err_word) {
+__device__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, const RowTask &task, int64_t row,
+                         int rp, bool skip, RowResult<R> &res, unsigned int *err_word) {
     using VL = VecLoad<BF16>;
     constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
-    constexpr int TE = TILE_BYTES / esz;
+    constexpr int CE = CHUNK_BYTES / esz;
     const int lane = threadIdx.x & 31;
-    const int cw = (threadIdx.x >> 5) - 1;
-    const int ctid = cw * 32 + lane;
+    const int w = ws.w;
     const int nsel = task.nsel;
 
     ScanState<R> st;
@@ -286,101 +304,106 @@ __device__ void scan_row(ScanSmem &sm, const ScanGeom &g, const RowTask &task, i
     st.set_tau(0);
 
     const char *rbase = g.base + row * g.ld_bytes;
-    for (int j = 0; j < g.tiles_per_row; ++j, ++it) {
-        const int stage = it % STAGES;
-        const bool quick = *reinterpret_cast<volatile int *>(&sm.abort_flag) != 0;
-        const bool ok = mbar_wait(&sm.full[stage], (it / STAGES) & 1, quick ? 0 : 2000000000ull);
-        if (!ok) {
-            st.bad = true;
-            if (lane == 0) {
-                atomicOr(err_word, ERR_WAIT_TIMEOUT);
-                *reinterpret_cast<volatile int *>(&sm.abort_flag) = 1;
+    for (int m = 0; m < ws.n_w; ++m) {
+        const int64_t k = ws.consumed;
+        const int stage = static_cast<int>(k % WSTAGES);
+        bool ok = !ws.aborted && mbar_wait(&sm.full[w][stage], static_cast<uint32_t>((k / WSTAGES) & 1),
+                                           WAIT_CYCLES);
+        ok = __all_sync(FULL, ok);
+        if (!ok && !ws.aborted) {
+            ws.aborted = true;
+            if (lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
+        }
+        if (!ok) st.bad = true;
+        if (ok) ws.consumed = k + 1;
+        const int c = w + SCAN_WARPS * m;
+        if (ok && !skip) {
+            if (MODE != MODE_ARGMAX) {
+                const uint64_t shared_tau = *reinterpret_cast<volatile unsigned long long *>(&sm.tau[rp]);
+                if (shared_tau > st.tau) st.set_tau(shared_tau);
             }
-        }
-        if (MODE != MODE_ARGMAX) {
-            const uint64_t shared_tau = *reinterpret_cast<volatile unsigned long long *>(&sm.tau[rp]);
-            if (shared_tau > st.tau) st.set_tau(shared_tau);
-        }
-        const int64_t e0 = static_cast<int64_t>(j) * TE;
-        int64_t cnt = g.V - e0;
-        if (cnt > TE) cnt = TE;
-        const int bulk = static_cast<int>((cnt * esz) & ~static_cast<int64_t>(15));
-        const unsigned char *tile = sm.tiles[stage];
+            const int64_t e0 = static_cast<int64_t>(c) * CE;
+            int64_t cnt = g.V - e0;
+            if (cnt > CE) cnt = CE;
+            const int bulk = static_cast<int>((cnt * esz) & ~static_cast<int64_t>(15));
+            const unsigned char *tile = sm.buf[w][stage];
 #pragma unroll
-        for (int q = 0; q < VEC_PER_THREAD; ++q) {
-            const int v = ctid + q * CTHREADS;
-            const bool valid = ok && v * 16 < bulk;
-            float x[VE];
-            float vmax = NEG_INF;
-            if (valid) {
-                VL::load(tile + v * 16, x, vmax);
-            } else {
+            for (int q = 0; q < VEC_PER_LANE; ++q) {
+                const int v = lane + q * 32;
+                const bool valid = v * 16 < bulk;
+                float x[VE];
+                float vmax = NEG_INF;
+                if (valid) {
+                    VL::load(tile + v * 16, x, vmax);
+                } else {
 #pragma unroll
-                for (int e = 0; e < VE; ++e) x[e] = NEG_INF;
+                    for (int e = 0; e < VE; ++e) x[e] = NEG_INF;
+                }
+                scan_vec<R, MODE, VE>(st, x, vmax, static_cast<uint32_t>(e0 + v * VE), valid, nsel, lane);
             }
-            scan_vec<R, MODE, VE>(st, x, vmax, static_cast<uint32_t>(e0 + v * VE), valid, nsel, lane);
-        }
-        // Ragged end of the row (fewer than 16 bytes): consumer warp 0, lane 0.
-        if (cw == 0 && bulk < cnt * esz) {
-            for (int64_t i = e0 + bulk / esz; i < e0 + cnt; ++i) {
-                const float xi = lane == 0 ? VL::scalar(rbase, i) : NEG_INF;
-                scan_one<R, MODE>(st, xi, static_cast<uint32_t>(i), lane == 0 && ok, nsel, lane);
+            // Ragged end of the row (fewer than 16 bytes), read by lane 0.
+            if (bulk < cnt * esz) {
+                for (int64_t i = e0 + bulk / esz; i < e0 + cnt; ++i) {
+                    const float xi = lane == 0 ? VL::scalar(rbase, i) : NEG_INF;
+                    scan_one<R, MODE>(st, xi, static_cast<uint32_t>(i), lane == 0, nsel, lane);
+                }
             }
+            if (MODE != MODE_ARGMAX && lane == 0 && st.tau != 0)
+                atomicMax(&sm.tau[rp], static_cast<unsigned long long>(st.tau));
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[stage]);
-        if (MODE != MODE_ARGMAX && lane == 0 && st.tau != 0)
-            atomicMax(&sm.tau[rp], static_cast<unsigned long long>(st.tau));
+        // Refill this stage with the item WSTAGES ahead (possibly of the next row).
+        if (ok && ws.issued < ws.total) stream_issue<esz>(sm, g, ws, ws.issued++, lane);
     }
 
-    // ---- merge the warps' results into consumer warp 0 ----
-    named_bar_sync(BAR_CONSUMERS, CTHREADS);  // A
-    if (ctid == 0) {
+    // ---- merge the warps' results into warp 0 ----
+    __syncthreads();  // A
+    if (threadIdx.x == 0) {
         sm.tau[rp ^ 1] = 0;
         sm.bad[rp ^ 1] = 0;
     }
     if (__any_sync(FULL, st.bad) && lane == 0) sm.bad[rp] = 1;
     if (MODE == MODE_ARGMAX) {
-        uint64_t k = st.bi >= 0 ? make_key(st.bv, static_cast<uint32_t>(st.bi)) : 0;
-        k = warp_max_u64(k);
-        if (lane == 0) sm.wbest[cw] = k;
+        uint64_t kb = st.bi >= 0 ? make_key(st.bv, static_cast<uint32_t>(st.bi)) : 0;
+        kb = warp_max_u64(kb);
+        if (lane == 0) sm.wbest[w] = kb;
     } else {
         if (MODE == MODE_TOPN_LSE) {
-            float m = st.m, s = st.s0 + st.s1;
+            float mm = st.m, s = st.s0 + st.s1;
 #pragma unroll
             for (int d = 16; d >= 1; d >>= 1) {
-                const float m2 = __shfl_xor_sync(FULL, m, d);
+                const float m2 = __shfl_xor_sync(FULL, mm, d);
                 const float s2 = __shfl_xor_sync(FULL, s, d);
-                lse_combine(m, s, m2, s2, st.c);
+                lse_combine(mm, s, m2, s2, st.c);
             }
             if (lane == 0) {
-                sm.wm[cw] = m;
-                sm.wsum[cw] = s;
+                sm.wm[w] = mm;
+                sm.wsum[w] = s;
             }
         }
-        st.list.store(sm.lists[cw], lane);
+        st.list.store(sm.lists[w], lane);
     }
-    named_bar_sync(BAR_CONSUMERS, CTHREADS);  // B
+    __syncthreads();  // B
     if (MODE != MODE_ARGMAX) {
         WarpList<R> o;
-        if ((cw & 1) == 0) {
-            o.load(sm.lists[cw + 1], lane);
+        if ((w & 1) == 0) {
+            o.load(sm.lists[w + 1], lane);
             st.list.merge(o, lane);
-            st.list.store(sm.lists[cw], lane);
+            st.list.store(sm.lists[w], lane);
         }
-        named_bar_sync(BAR_CONSUMERS, CTHREADS);
-        if ((cw & 3) == 0) {
-            o.load(sm.lists[cw + 2], lane);
+        __syncthreads();
+        if ((w & 3) == 0) {
+            o.load(sm.lists[w + 2], lane);
             st.list.merge(o, lane);
-            st.list.store(sm.lists[cw], lane);
+            st.list.store(sm.lists[w], lane);
         }
-        named_bar_sync(BAR_CONSUMERS, CTHREADS);
-        if (cw == 0) {
+        __syncthreads();
+        if (w == 0) {
             o.load(sm.lists[4], lane);
             st.list.merge(o, lane);
         }
     }
-    if (cw == 0) {
+    if (w == 0) {
         res.bad = sm.bad[rp] != 0;
         res.list = st.list;
         res.best = 0;
@@ -388,13 +411,13 @@ __device__ void scan_row(ScanSmem &sm, const ScanGeom &g, const RowTask &task, i
         res.s = 0.0f;
         if (MODE == MODE_ARGMAX) {
             uint64_t b = 0;
-            for (int w = 0; w < CWARPS; ++w) b = sm.wbest[w] > b ? sm.wbest[w] : b;
+            for (int i = 0; i < SCAN_WARPS; ++i) b = sm.wbest[i] > b ? sm.wbest[i] : b;
             res.best = b;
         }
         if (MODE == MODE_TOPN_LSE) {
-            float m = sm.wm[0], s = sm.wsum[0];
-            for (int w = 1; w < CWARPS; ++w) lse_combine(m, s, sm.wm[w], sm.wsum[w], st.c);
-            res.m = m;
+            float mm = sm.wm[0], s = sm.wsum[0];
+            for (int i = 1; i < SCAN_WARPS; ++i) lse_combine(mm, s, sm.wm[i], sm.wsum[i], st.c);
+            res.m = mm;
             res.s = s;
         }
     }
@@ -402,13 +425,10 @@ __device__ void scan_row(ScanSmem &sm, const ScanGeom &g, const RowTask &task, i
 
 __device__ __forceinline__ void scan_init(ScanSmem &sm) {
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&sm.full[s], 1);
-            mbar_init(&sm.empty[s], CWARPS);
-        }
+        for (int w = 0; w < SCAN_WARPS; ++w)
+            for (int s = 0; s < WSTAGES; ++s) mbar_init(&sm.full[w][s], 1);
         sm.tau[0] = sm.tau[1] = 0;
         sm.bad[0] = sm.bad[1] = 0;
-        sm.abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();

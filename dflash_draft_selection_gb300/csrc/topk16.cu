@@ -54,24 +54,24 @@ __device__ void finalize_draft(const RowResult<R> &res, const RowTask &task, int
 }
 
 template <int R, bool BF16>
-__global__ void __launch_bounds__(SCAN_THREADS) k_topk16(ScanGeom g, int32_t *cand_idx, float *cand_U,
+__global__ void __launch_bounds__(SCAN_THREADS, 3) k_topk16(ScanGeom g, int32_t *cand_idx, float *cand_U,
                                                          float *lse) {
     extern __shared__ unsigned char smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-    scan_init(sm);
-    if (threadIdx.x < 32) {
-        scan_producer<BF16>(sm, g, &g_err_topk);
-        return;
-    }
+    constexpr int esz = BF16 ? 2 : 4;
     const int lane = threadIdx.x & 31;
-    const int cw = (threadIdx.x >> 5) - 1;
-    uint32_t it = 0;
+    const int w = threadIdx.x >> 5;
+    scan_init(sm);
+    WarpStream ws;
+    stream_start<esz>(sm, g, ws, lane);
     int rp = 0;
-    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x) {
+    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x, rp ^= 1) {
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, false);
+        RowResult<R> res;
         if (!row_streams(task)) {
-            if (cw == 0) {
+            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rp, true, res, &g_err_topk);
+            if (w == 0) {
                 if (lane < NC) {
                     cand_idx[row * NC + lane] = -1;
                     cand_U[row * NC + lane] = NAN;
@@ -80,20 +80,19 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_topk16(ScanGeom g, int32_t *ca
             }
             continue;
         }
-        RowResult<R> res;
         if (task.mode == MODE_TOPN_LSE)
-            scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, task, row, it, rp, res, &g_err_topk);
+            scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_topk);
         else
-            scan_row<R, MODE_TOPN, BF16>(sm, g, task, row, it, rp, res, &g_err_topk);
-        if (cw == 0) finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
-        rp ^= 1;
+            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_topk);
+        if (w == 0) finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
     }
+    if (ws.aborted) stream_drain(sm, ws);
 }
 
 template <int R, bool BF16>
 static dflash2_status launch_topk16(const ScanGeom &g, int32_t *cand_idx, float *cand_U, float *lse,
                                     cudaStream_t stream) {
-    const size_t smem = sizeof(ScanSmem) + 128;
+    const size_t smem = scan_smem_bytes();
     const void *fn = reinterpret_cast<const void *>(&k_topk16<R, BF16>);
     const int per_sm = blocks_per_sm(fn, SCAN_THREADS, smem);
     int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
@@ -133,7 +132,7 @@ extern "C" dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, i
     g.ld_bytes = ld * es;
     g.V = V;
     g.rows = rows;
-    g.tiles_per_row = static_cast<int>((V * es + TILE_BYTES - 1) / TILE_BYTES);
+    g.chunks_per_row = static_cast<int>((V * es + CHUNK_BYTES - 1) / CHUNK_BYTES);
     g.params = params;
     g.rows_per_param = rows_per_param;
     g.target = false;

@@ -283,26 +283,26 @@ __device__ void row_done(const VerifyArgs &a, const dflash2_sampling *params, in
 }
 
 template <int R, bool BF16>
-__global__ void __launch_bounds__(SCAN_THREADS) k_verify(ScanGeom g, VerifyArgs a) {
+__global__ void __launch_bounds__(SCAN_THREADS, 3) k_verify(ScanGeom g, VerifyArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(base);
     DrawScratch &sc = *reinterpret_cast<DrawScratch *>(base + sizeof(ScanSmem));
-    scan_init(sm);
-    if (threadIdx.x < 32) {
-        scan_producer<BF16>(sm, g, &g_err_verify);
-        return;
-    }
+    constexpr int esz = BF16 ? 2 : 4;
     const int lane = threadIdx.x & 31;
-    const int cw = (threadIdx.x >> 5) - 1;
-    uint32_t it = 0;
+    const int w = threadIdx.x >> 5;
+    scan_init(sm);
+    WarpStream ws;
+    stream_start<esz>(sm, g, ws, lane);
     int rp = 0;
-    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x) {
+    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x, rp ^= 1) {
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
         TRec *rec = a.recs + row;
+        RowResult<R> res;
         if (!row_streams(task)) {
-            if (cw == 0) {
+            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rp, true, res, &g_err_verify);
+            if (w == 0) {
                 if (lane == 0) {
                     rec->n = 0;
                     rec->flags = task.status;
@@ -311,22 +311,21 @@ __global__ void __launch_bounds__(SCAN_THREADS) k_verify(ScanGeom g, VerifyArgs 
             }
             continue;
         }
-        RowResult<R> res;
         if (task.mode == MODE_ARGMAX)
-            scan_row<R, MODE_ARGMAX, BF16>(sm, g, task, row, it, rp, res, &g_err_verify);
+            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_verify);
         else
-            scan_row<R, MODE_TOPN, BF16>(sm, g, task, row, it, rp, res, &g_err_verify);
-        if (cw == 0) {
+            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_verify);
+        if (w == 0) {
             finalize_target<R>(res, task, rec, lane);
             row_done(a, g.params, row, g.V, sc, lane);
         }
-        rp ^= 1;
     }
+    if (ws.aborted) stream_drain(sm, ws);
 }
 
 template <int R, bool BF16>
 static dflash2_status launch_verify(const ScanGeom &g, const VerifyArgs &a, cudaStream_t stream) {
-    const size_t smem = sizeof(ScanSmem) + sizeof(DrawScratch) + 128;
+    const size_t smem = scan_smem_bytes() + sizeof(DrawScratch);
     const void *fn = reinterpret_cast<const void *>(&k_verify<R, BF16>);
     const int per_sm = blocks_per_sm(fn, SCAN_THREADS, smem);
     int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
@@ -383,7 +382,7 @@ extern "C" dflash2_status dflash2_verify(const void *tlogits, dflash2_dtype dt, 
     g.ld_bytes = ld * es;
     g.V = V;
     g.rows = B * (K + 1);
-    g.tiles_per_row = static_cast<int>((V * es + TILE_BYTES - 1) / TILE_BYTES);
+    g.chunks_per_row = static_cast<int>((V * es + CHUNK_BYTES - 1) / CHUNK_BYTES);
     g.params = params;
     g.rows_per_param = K + 1;
     g.target = true;

@@ -35,3 +35,13 @@ def assert_close(gpu, ref, rtol=RTOL, atol=ATOL, what=""):
 def params_np(B, T, k, p):
     from dflash_draft_selection_gb300 import synth
     return synth.make_params(B, T, k, p)
+
+
+def padded(z):
+    """z [rows, V] copied into rows whose stride is a multiple of 16 bytes (the ABI's row alignment)."""
+    rows, V = z.shape
+    per = 16 // z.element_size()
+    ld = (V + per - 1) // per * per
+    buf = torch.zeros(rows, ld, dtype=z.dtype, device=z.device)
+    buf[:, :V] = z
+    return buf[:, :V]

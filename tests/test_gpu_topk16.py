@@ -5,14 +5,14 @@ import torch
 
 import dflash_draft_selection_gb300 as d2
 from dflash_draft_selection_gb300 import synth
-from tests._util import MARGIN, assert_close, cuda_or_skip, params_np
+from tests._util import MARGIN, assert_close, cuda_or_skip, padded, params_np
 
 pytestmark = pytest.mark.gpu
 
 
 def run_both(ref, z, params=None, rpp=1, V=None):
     dev = cuda_or_skip()
-    zg = z.to(dev)
+    zg = padded(z.to(dev))
     pg = None if params is None else d2.sampling_params(params["temperature"], params["top_k"], params["top_p"],
                                                         device=dev)
     Vv = z.shape[1] if V is None else V

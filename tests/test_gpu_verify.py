@@ -7,7 +7,7 @@ import torch
 
 import dflash_draft_selection_gb300 as d2
 from dflash_draft_selection_gb300 import synth
-from tests._util import MARGIN, cuda_or_skip, params_np
+from tests._util import MARGIN, cuda_or_skip, padded, params_np
 
 pytestmark = pytest.mark.gpu
 
@@ -25,7 +25,7 @@ def run_gpu_verify(inp, cand, pt, ps, q, params, B, K, trusted=False, V=None):
     pg = None if params is None else d2.sampling_params(params["temperature"], params["top_k"], params["top_p"],
                                                         device=dev)
     t = lambda a, dt: torch.as_tensor(np.ascontiguousarray(a)).to(dt).to(dev)
-    acc, out, st = d2.verify(inp.target_logits.to(dev), t(pt, torch.int32), t(cand, torch.int32),
+    acc, out, st = d2.verify(padded(inp.target_logits.to(dev)), t(pt, torch.int32), t(cand, torch.int32),
                              t(q, torch.float32), t(ps, torch.int32), params=pg, u_acc=inp.u_acc.to(dev),
                              u_res=inp.u_res.to(dev), trusted=trusted, V=V)
     torch.cuda.synchronize()
