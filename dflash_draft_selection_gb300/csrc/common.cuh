@@ -41,14 +41,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+// One bounded poll of an mbarrier phase: the thread may be suspended for at
+// most about 20 us while the phase is incomplete.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(20000u)
         : "memory");
     return ok != 0;
 }
@@ -60,11 +62,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
                                           long long max_cycles = 4000000000ll) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
-    for (;;) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > max_cycles) return false;
-    }
+    while (clock64() - t0 <= max_cycles)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
 }
 
 // Order this thread's earlier generic-proxy accesses to shared memory before

@@ -10,7 +10,7 @@
 // that consumes a stage is the one that refills it, so no cross-warp
 // handshake is needed.  Each thread keeps the running max and sum of
 // exponentials (or argmax) of its elements, each warp a register-resident
-// list of its best keys filtered by a CTA-wide threshold.  At the end of a
+// list of its best keys filtered by a CTA-wide threshold value.  At the end of a
 // row the warp results are merged (bitonic networks) and warp 0 holds the
 // row result.  Waits are bounded: a warp that times out raises the error
 // word, stops issuing copies, waits a bounded time for those in flight and
@@ -43,7 +43,7 @@ struct ScanGeom {
 
 struct ScanSmem {
     uint64_t full[SCAN_WARPS][WSTAGES];
-    unsigned long long tau[2];
+    unsigned int tau_ord[2];  // CTA-wide threshold: ordered value bits of the best warp's N-th key
     int bad[2];
     float wm[SCAN_WARPS];
     float wsum[SCAN_WARPS];
@@ -122,9 +122,10 @@ struct ScanState {
     float bv;
     int32_t bi;
     float m, s0, s1, negmc, c;
-    uint64_t tau;
+    uint64_t tau;     // this warp's N-th best key (0 while the list is short)
     float tau_val;
     uint32_t tau_idx;
+    float sval;       // CTA-wide threshold value: no element below it can be in the top N
     bool bad;
     WarpList<R> list;
 
@@ -145,13 +146,13 @@ struct ScanState {
 template <int R, int VE>
 __device__ __forceinline__ void offer_topn(ScanState<R> &st, const float (&x)[VE], float vmax,
                                            uint32_t idx0, bool valid, int nsel, int lane) {
-    const bool maybe = valid && vmax >= st.tau_val;
+    const bool maybe = valid && vmax >= fmaxf(st.tau_val, st.sval);
     if (!__any_sync(FULL, maybe)) return;
 #pragma unroll
     for (int e = 0; e < VE; ++e) {
         const float xe = x[e];
         const uint32_t ie = idx0 + e;
-        const bool c = maybe && (xe > st.tau_val || (xe == st.tau_val && ie < st.tau_idx));
+        const bool c = maybe && xe >= st.sval && (xe > st.tau_val || (xe == st.tau_val && ie < st.tau_idx));
         uint32_t msk = __ballot_sync(FULL, c);
         while (msk) {
             const int l = __ffs(msk) - 1;
@@ -222,7 +223,7 @@ __device__ __forceinline__ void scan_one(ScanState<R> &st, float x, uint32_t idx
         }
         if (st.m != NEG_INF) st.s0 += ex2(fmaf(x, st.c, st.negmc));
     }
-    const bool c = valid && (x > st.tau_val || (x == st.tau_val && idx < st.tau_idx));
+    const bool c = valid && x >= st.sval && (x > st.tau_val || (x == st.tau_val && idx < st.tau_idx));
     uint32_t msk = __ballot_sync(FULL, c);
     while (msk) {
         const int l = __ffs(msk) - 1;
@@ -302,6 +303,7 @@ __device__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, const 
     st.bad = false;
     st.list.clear();
     st.set_tau(0);
+    st.sval = NEG_INF;
 
     const char *rbase = g.base + row * g.ld_bytes;
     for (int m = 0; m < ws.n_w; ++m) {
@@ -319,8 +321,8 @@ __device__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, const 
         const int c = w + SCAN_WARPS * m;
         if (ok && !skip) {
             if (MODE != MODE_ARGMAX) {
-                const uint64_t shared_tau = *reinterpret_cast<volatile unsigned long long *>(&sm.tau[rp]);
-                if (shared_tau > st.tau) st.set_tau(shared_tau);
+                const uint32_t so = *reinterpret_cast<volatile unsigned int *>(&sm.tau_ord[rp]);
+                if (so != 0) st.sval = fmaxf(st.sval, ord2f(so));
             }
             const int64_t e0 = static_cast<int64_t>(c) * CE;
             int64_t cnt = g.V - e0;
@@ -348,8 +350,9 @@ __device__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, const 
                     scan_one<R, MODE>(st, xi, static_cast<uint32_t>(i), lane == 0, nsel, lane);
                 }
             }
+            // Publish the warp's N-th value (32-bit: a native shared-memory max).
             if (MODE != MODE_ARGMAX && lane == 0 && st.tau != 0)
-                atomicMax(&sm.tau[rp], static_cast<unsigned long long>(st.tau));
+                atomicMax(&sm.tau_ord[rp], static_cast<uint32_t>(st.tau >> 32));
         }
         __syncwarp();
         // Refill this stage with the item WSTAGES ahead (possibly of the next row).
@@ -359,7 +362,7 @@ __device__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, const 
     // ---- merge the warps' results into warp 0 ----
     __syncthreads();  // A
     if (threadIdx.x == 0) {
-        sm.tau[rp ^ 1] = 0;
+        sm.tau_ord[rp ^ 1] = 0;
         sm.bad[rp ^ 1] = 0;
     }
     if (__any_sync(FULL, st.bad) && lane == 0) sm.bad[rp] = 1;
@@ -427,7 +430,7 @@ __device__ __forceinline__ void scan_init(ScanSmem &sm) {
     if (threadIdx.x == 0) {
         for (int w = 0; w < SCAN_WARPS; ++w)
             for (int s = 0; s < WSTAGES; ++s) mbar_init(&sm.full[w][s], 1);
-        sm.tau[0] = sm.tau[1] = 0;
+        sm.tau_ord[0] = sm.tau_ord[1] = 0;
         sm.bad[0] = sm.bad[1] = 0;
         fence_barrier_init();
     }
