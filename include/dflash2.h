@@ -158,6 +158,38 @@ dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand
                                        dflash2_stream stream);
 
 /*
+ * dflash2_pair_score_walk_noalloc -- no counterpart on the pages: an addition
+ * of this library.  The same computation and arguments as
+ * dflash2_pair_score_walk, without the workspace, for callers that cannot
+ * give this library device memory: for example a plugin or an engine whose
+ * memory pool owns all device memory and offers no scratch to the code it
+ * calls, or code that may not call an allocator at the point where the
+ * selector runs.  The scratch (one ticket per request) is a fixed array in
+ * the library's own device memory, DFLASH2_WALK_NOALLOC_MAX_B tickets (64 KB)
+ * held by every GPU that loads the library until the process exits.
+ *   - B > DFLASH2_WALK_NOALLOC_MAX_B returns DFLASH2_ERR_WORKSPACE and
+ *     launches nothing; other argument errors are those of
+ *     dflash2_pair_score_walk.
+ *   - Nothing is allocated: each call clears its share of the array
+ *     (cudaMemsetAsync on `stream`) and then launches the kernel.
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array: two calls that may overlap on the GPU
+ *     (different streams, or different host threads) race and give wrong
+ *     paths.  Order them on one stream or synchronise between them.
+ */
+#define DFLASH2_WALK_NOALLOC_MAX_B 16384
+dflash2_status dflash2_pair_score_walk_noalloc(int64_t B, int32_t K, const int32_t *cand_idx,
+                                               const float *cand_U, const int32_t *last_tok,
+                                               const void *A, const void *Bt, dflash2_dtype tdt,
+                                               int64_t V, int32_t D, const float *gate,
+                                               const dflash2_sampling *params,
+                                               const float *u_walk, int32_t *path_tok,
+                                               int32_t *path_slot, float *q_sel, float *scores,
+                                               dflash2_stream stream);
+
+/*
  * dflash2_verify -- [F] Sampled verify (accept with min(1, p/q); on a reject
  * resample from max(0, p - q); all-greedy batches keep the prefix match);
  * [P] "Proposal" phase 3; [F] "Tests added or changed" (trusted, NaN,
