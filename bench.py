@@ -173,6 +173,7 @@ class Chain:
         self.pt, self.ps = e(B, K, dt=torch.int32), e(B, K, dt=torch.int32)
         self.q, self.S = e(B, K, 16), e(B, K, 16, 16)
         self.acc, self.out, self.st = e(B, dt=torch.int32), e(B, K + 1, dt=torch.int32), e(B, dt=torch.int32)
+        self.ws_topk = d2.Workspace.for_topk16(B * K, dev)
         self.ws_walk = d2.Workspace.for_walk(B, dev)
         self.ws_verify = d2.Workspace.for_verify(B, K, dev)
 
@@ -180,7 +181,8 @@ class Chain:
         d2, B, K = self.d2, self.shp.B, self.shp.K
         pg = self.params
         if which == "k_topk16":
-            d2.topk16(inp.draft_logits, params=pg, rows_per_param=K, out=(self.cand, self.U, self.lse))
+            d2.topk16(inp.draft_logits, params=pg, rows_per_param=K, ws=self.ws_topk,
+                      out=(self.cand, self.U, self.lse))
         elif which == "k_gate_tc":
             d2.ctx_gate(inp.h, self.Wg, out=self.gate)
         elif which == "k_pair_score_walk":

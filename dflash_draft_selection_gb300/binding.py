@@ -46,7 +46,9 @@ def load_library():
             raise OSError(f"{LIB_PATH} is missing: build it with `python -m dflash_draft_selection_gb300.build`")
         L = ctypes.CDLL(LIB_PATH)
         vp, i64, i32, u32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint32, ctypes.c_size_t
-        L.dflash2_topk16.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp]
+        L.dflash2_topk16_workspace_bytes.argtypes = [i64]
+        L.dflash2_topk16_workspace_bytes.restype = sz
+        L.dflash2_topk16.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp, sz, vp]
         L.dflash2_ctx_gate.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp]
         L.dflash2_pair_score_walk_workspace_bytes.argtypes = [i64]
         L.dflash2_pair_score_walk_workspace_bytes.restype = sz
@@ -133,6 +135,10 @@ class Workspace:
         return ctypes.c_void_p(self.buf.data_ptr())
 
     @staticmethod
+    def for_topk16(rows: int, device="cuda") -> "Workspace":
+        return Workspace(load_library().dflash2_topk16_workspace_bytes(rows), device)
+
+    @staticmethod
     def for_walk(B: int, device="cuda") -> "Workspace":
         return Workspace(load_library().dflash2_pair_score_walk_workspace_bytes(B), device)
 
@@ -142,7 +148,7 @@ class Workspace:
 
 
 # ------------------------------------------------------------------ calls ----
-def topk16(logits: torch.Tensor, params=None, rows_per_param: int = 1, V: int | None = None, out=None):
+def topk16(logits: torch.Tensor, params=None, rows_per_param: int = 1, V: int | None = None, ws=None, out=None):
     """dflash2_topk16.  logits [rows, ld] (bf16/f32).  Returns (cand_idx, cand_U, lse)."""
     L = load_library()
     _need_cuda(logits)
@@ -155,9 +161,12 @@ def topk16(logits: torch.Tensor, params=None, rows_per_param: int = 1, V: int | 
                torch.empty(rows, NC, dtype=torch.float32, device=dev),
                torch.empty(rows, dtype=torch.float32, device=dev))
     cand_idx, cand_U, lse = out
+    if ws is None:
+        ws = Workspace.for_topk16(rows, dev)
     p = _params_from(params, dev)
     _check("dflash2_topk16", L.dflash2_topk16(_ptr(logits), _dtype(logits), rows, V, ld, _ptr(p), rows_per_param,
-                                              _ptr(cand_idx), _ptr(cand_U), _ptr(lse), _stream(dev)))
+                                              _ptr(cand_idx), _ptr(cand_U), _ptr(lse), ws.ptr(), ws.nbytes,
+                                              _stream(dev)))
     return cand_idx, cand_U, lse
 
 

@@ -14,7 +14,7 @@ namespace dfl {
 static __device__ unsigned int g_err_topk;
 
 template <int R>
-__device__ void finalize_draft(const RowResult<R> &res, const RowTask &task, int64_t row,
+__device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const RowTask &task, int64_t row,
                                int32_t *cand_idx, float *cand_U, float *lse, int lane) {
     const uint64_t k = res.list.k[0];
     const float z = key_val(k);
@@ -53,51 +53,63 @@ __device__ void finalize_draft(const RowResult<R> &res, const RowTask &task, int
     if (lane == 0) lse[row] = L;
 }
 
-template <int R, bool BF16>
-__global__ void __launch_bounds__(SCAN_THREADS, 3) k_topk16(ScanGeom g, int32_t *cand_idx, float *cand_U,
-                                                         float *lse) {
+// SAMPLED: some request may sample (params given): lists of 64 keys and every
+// row mode; otherwise every row is greedy (top-16 and the log normaliser).
+template <bool SAMPLED, bool BF16>
+__global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_topk16(ScanGeom g, ScanWs sw,
+                                                                                  int32_t *cand_idx,
+                                                                                  float *cand_U, float *lse) {
+    constexpr int R = SAMPLED ? 2 : 1;
     extern __shared__ unsigned char smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
-    constexpr int esz = BF16 ? 2 : 4;
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     scan_init(sm);
+    const int64_t begin = range_begin(g, blockIdx.x), end = range_begin(g, blockIdx.x + 1);
     WarpStream ws;
-    stream_start<esz>(sm, g, ws, lane);
-    int rp = 0;
-    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x, rp ^= 1) {
+    stream_start(sm, g, ws, begin, end, w, lane);
+    const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
+    for (int64_t row = r_first; row <= r_last; ++row) {
+        const int rrel = static_cast<int>(row - r_first), rp = rrel & 1;
+        int w0;
+        const int expect = row_warps(g, row, begin, end, &w0);
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, false);
         RowResult<R> res;
-        if (!row_streams(task)) {
-            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rp, true, res, &g_err_topk);
-            if (w == 0) {
+        if (!SAMPLED || task.mode == MODE_TOPN_LSE) {
+            scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_topk);
+            if (w == 0 && join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, LOG2E / task.T, lane)) {
+                if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, lane);
+                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
+            }
+        } else if (task.mode == MODE_TOPN) {
+            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_topk);
+            if (w == 0 && join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E / task.T, lane)) {
+                if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, lane);
+                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
+            }
+        } else {
+            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, true, res, &g_err_topk);
+            if (w == 0 && blockIdx.x == range_owner(g, row * g.cpr)) {
                 if (lane < NC) {
                     cand_idx[row * NC + lane] = -1;
                     cand_U[row * NC + lane] = NAN;
                 }
                 if (lane == 0) lse[row] = NAN;
             }
-            continue;
         }
-        if (task.mode == MODE_TOPN_LSE)
-            scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_topk);
-        else
-            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_topk);
-        if (w == 0) finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
     }
-    if (ws.aborted) stream_drain(sm, ws);
+    if (ws.aborted) stream_drain(sm, ws, w);
 }
 
-template <int R, bool BF16>
-static dflash2_status launch_topk16(const ScanGeom &g, int32_t *cand_idx, float *cand_U, float *lse,
-                                    cudaStream_t stream) {
+template <bool SAMPLED, bool BF16>
+static dflash2_status launch_topk16(const ScanGeom &g, const ScanWs &sw, int32_t *cand_idx, float *cand_U,
+                                    float *lse, cudaStream_t stream) {
     const size_t smem = scan_smem_bytes();
-    const void *fn = reinterpret_cast<const void *>(&k_topk16<R, BF16>);
-    const int per_sm = blocks_per_sm(fn, SCAN_THREADS, smem);
-    int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
-    if (grid > g.rows) grid = g.rows;
-    k_topk16<R, BF16><<<static_cast<unsigned>(grid), SCAN_THREADS, smem, stream>>>(g, cand_idx, cand_U, lse);
+    const void *fn = reinterpret_cast<const void *>(&k_topk16<SAMPLED, BF16>);
+    const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.total);
+    k_topk16<SAMPLED, BF16><<<static_cast<unsigned>(grid), SCAN_THREADS, smem, stream>>>(g, sw, cand_idx, cand_U,
+                                                                                       lse);
     return after_launch();
 }
 
@@ -115,31 +127,31 @@ unsigned int read_error_topk(bool clear) {
 
 using namespace dfl;
 
+extern "C" size_t dflash2_topk16_workspace_bytes(int64_t rows) {
+    if (rows < 0) return 0;
+    return scan_ws_bytes(rows);
+}
+
 extern "C" dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
                                          int64_t ld, const dflash2_sampling *params,
                                          int64_t rows_per_param, int32_t *cand_idx, float *cand_U,
-                                         float *lse, dflash2_stream stream) {
+                                         float *lse, void *ws, size_t ws_bytes, dflash2_stream stream) {
     if (!dtype_ok(dt) || rows < 0 || V < NC || V >= (int64_t(1) << 31) || ld < V || rows_per_param < 1)
         return DFLASH2_ERR_INVALID_ARG;
     const int es = esize(dt);
     if ((ld * es) % 16 != 0) return DFLASH2_ERR_INVALID_ARG;
     if (rows == 0) return DFLASH2_OK;
-    if (!logits || !cand_idx || !cand_U || !lse || !aligned16(logits) || !aligned16(cand_idx) ||
-        !aligned16(cand_U) || !aligned16(lse) || (params && (reinterpret_cast<uintptr_t>(params) & 3)))
+    if (!logits || !cand_idx || !cand_U || !lse || !ws || !aligned16(logits) || !aligned16(cand_idx) ||
+        !aligned16(cand_U) || !aligned16(lse) || !aligned16(ws) ||
+        (params && (reinterpret_cast<uintptr_t>(params) & 3)))
         return DFLASH2_ERR_INVALID_ARG;
-    ScanGeom g;
-    g.base = static_cast<const char *>(logits);
-    g.ld_bytes = ld * es;
-    g.V = V;
-    g.rows = rows;
-    g.chunks_per_row = static_cast<int>((V * es + CHUNK_BYTES - 1) / CHUNK_BYTES);
-    g.params = params;
-    g.rows_per_param = rows_per_param;
-    g.target = false;
+    if (ws_bytes < scan_ws_bytes(rows)) return DFLASH2_ERR_WORKSPACE;
+    const ScanGeom g = make_geom(logits, ld, es, V, rows, params, rows_per_param);
+    const ScanWs sw = scan_ws_at(ws, rows);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (params == nullptr)
-        return dt == DFLASH2_BF16 ? launch_topk16<1, true>(g, cand_idx, cand_U, lse, s)
-                                  : launch_topk16<1, false>(g, cand_idx, cand_U, lse, s);
-    return dt == DFLASH2_BF16 ? launch_topk16<2, true>(g, cand_idx, cand_U, lse, s)
-                              : launch_topk16<2, false>(g, cand_idx, cand_U, lse, s);
+        return dt == DFLASH2_BF16 ? launch_topk16<false, true>(g, sw, cand_idx, cand_U, lse, s)
+                                  : launch_topk16<false, false>(g, sw, cand_idx, cand_U, lse, s);
+    return dt == DFLASH2_BF16 ? launch_topk16<true, true>(g, sw, cand_idx, cand_U, lse, s)
+                              : launch_topk16<true, false>(g, sw, cand_idx, cand_U, lse, s);
 }

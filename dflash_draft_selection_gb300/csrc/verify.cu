@@ -48,7 +48,7 @@ constexpr size_t TICKET_BYTES_ALIGN = 256;
 
 // ---------------------------------------------------------------- records --
 template <int R>
-__device__ void finalize_target(const RowResult<R> &res, const RowTask &task, TRec *rec, int lane) {
+__device__ __forceinline__ void finalize_target(const RowResult<R> &res, const RowTask &task, TRec *rec, int lane) {
     int32_t flags = DFLASH2_ST_OK;
     if (task.mode == MODE_ARGMAX) {
         const bool bad = res.bad || res.best == 0 || !isfinite(key_val(res.best));
@@ -89,6 +89,7 @@ struct DrawScratch {
     int32_t sid[DFLASH2_MAX_TOPK];
     float sw[DFLASH2_MAX_TOPK];
 };
+static_assert(sizeof(DrawScratch) <= sizeof(ScanSmem::lists), "the draw scratch lives in the list slots");
 
 // Inverse CDF over the entries sorted by ascending token id: the first entry
 // whose running weight exceeds u * (total weight); if rounding leaves none,
@@ -145,21 +146,34 @@ __device__ __forceinline__ float ldcg_f(const float *p) { return __ldcg(p); }
 
 // The accept walk of request b (consumer warp 0 of the CTA that completed the
 // request's rows).
+template <bool SAMPLED>
 __device__ void accept_request(const VerifyArgs &a, const dflash2_sampling *params, int64_t b,
                                int64_t V, DrawScratch &sc, int lane) {
     const int K = a.K;
     const RowTask rt = decode_row(params, b, V, true);
-    const bool greedy = rt.mode == MODE_ARGMAX;
+    const bool greedy = !SAMPLED || rt.mode == MODE_ARGMAX;
     const TRec *rec = a.recs + b * (K + 1);
     int st = DFLASH2_ST_OK;
     if (rt.mode == MODE_SKIP) {
         st = rt.status;
     } else {
-        for (int t = 0; t <= K; ++t)
-            if (ldcg_i(&rec[t].flags) != DFLASH2_ST_OK) {
-                st = DFLASH2_ST_NAN;
-                break;
-            }
+        const int32_t fl = lane <= K ? ldcg_i(&rec[lane].flags) : DFLASH2_ST_OK;
+        if (__any_sync(FULL, fl != DFLASH2_ST_OK)) st = DFLASH2_ST_NAN;
+    }
+    if (st == DFLASH2_ST_OK && greedy) {
+        // All rows at once: lane t holds the target argmax of row t and the
+        // drafted token of position t; the first mismatch ends the prefix.
+        const int32_t g = lane <= K ? ldcg_i(&rec[lane].ids[0]) : -1;
+        const int32_t d = lane < K ? a.path_tok[b * K + lane] : -1;
+        const uint32_t miss = __ballot_sync(FULL, lane < K && d != g);
+        const int n = miss ? __ffs(miss) - 1 : K;
+        const int32_t emit = __shfl_sync(FULL, g, n);
+        for (int i = lane; i <= K; i += 32) a.out_tok[b * (K + 1) + i] = i < n ? a.path_tok[b * K + i] : (i == n ? emit : -1);
+        if (lane == 0) {
+            a.accept_len[b] = n;
+            a.status[b] = DFLASH2_ST_OK;
+        }
+        return;
     }
     if (st == DFLASH2_ST_OK && !greedy) {
         for (int t = 0; t < K; ++t) {
@@ -267,6 +281,7 @@ __device__ void accept_request(const VerifyArgs &a, const dflash2_sampling *para
 
 // Publish the row's record and, if it was the request's last row, run the
 // accept walk.  Consumer warp 0.
+template <bool SAMPLED>
 __device__ void row_done(const VerifyArgs &a, const dflash2_sampling *params, int64_t row,
                          int64_t V, DrawScratch &sc, int lane) {
     const int64_t b = row / (a.K + 1);
@@ -278,59 +293,71 @@ __device__ void row_done(const VerifyArgs &a, const dflash2_sampling *params, in
     if (old == a.K) {
         if (lane == 0) a.tickets[b] = 0;
         __threadfence();
-        accept_request(a, params, b, V, sc, lane);
+        accept_request<SAMPLED>(a, params, b, V, sc, lane);
     }
 }
 
-template <int R, bool BF16>
-__global__ void __launch_bounds__(SCAN_THREADS, 3) k_verify(ScanGeom g, VerifyArgs a) {
+// SAMPLED: some request may sample (params given); otherwise every row is
+// an argmax and every request greedy.
+template <bool SAMPLED, bool BF16>
+__global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_verify(ScanGeom g, ScanWs sw,
+                                                                                  VerifyArgs a) {
+    constexpr int R = SAMPLED ? 2 : 1;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(base);
-    DrawScratch &sc = *reinterpret_cast<DrawScratch *>(base + sizeof(ScanSmem));
-    constexpr int esz = BF16 ? 2 : 4;
+    // The accept walk runs on warp 0 between two rows, while the per-warp
+    // list slots are idle (they are written again only after the next row's
+    // first barrier, which warp 0 reaches after the walk).
+    DrawScratch &sc = *reinterpret_cast<DrawScratch *>(&sm.lists[0][0]);
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     scan_init(sm);
+    const int64_t begin = range_begin(g, blockIdx.x), end = range_begin(g, blockIdx.x + 1);
     WarpStream ws;
-    stream_start<esz>(sm, g, ws, lane);
-    int rp = 0;
-    for (int64_t row = blockIdx.x; row < g.rows; row += gridDim.x, rp ^= 1) {
+    stream_start(sm, g, ws, begin, end, w, lane);
+    const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
+    for (int64_t row = r_first; row <= r_last; ++row) {
+        const int rrel = static_cast<int>(row - r_first), rp = rrel & 1;
+        int w0;
+        const int expect = row_warps(g, row, begin, end, &w0);
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
         TRec *rec = a.recs + row;
         RowResult<R> res;
-        if (!row_streams(task)) {
-            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rp, true, res, &g_err_verify);
-            if (w == 0) {
+        bool done = false;
+        if (!SAMPLED || task.mode == MODE_ARGMAX) {
+            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_verify);
+            done = w == 0 && join_parts<R, MODE_ARGMAX>(g, sw, row, res, LOG2E, lane);
+        } else if (task.mode == MODE_TOPN) {
+            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_verify);
+            done = w == 0 && join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
+            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, lane);
+        } else {
+            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, true, res, &g_err_verify);
+            if (w == 0 && blockIdx.x == range_owner(g, row * g.cpr)) {
                 if (lane == 0) {
                     rec->n = 0;
                     rec->flags = task.status;
                 }
-                row_done(a, g.params, row, g.V, sc, lane);
+                row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
             }
-            continue;
         }
-        if (task.mode == MODE_ARGMAX)
-            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_verify);
-        else
-            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rp, false, res, &g_err_verify);
-        if (w == 0) {
+        if (done) {
             finalize_target<R>(res, task, rec, lane);
-            row_done(a, g.params, row, g.V, sc, lane);
+            row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
         }
     }
-    if (ws.aborted) stream_drain(sm, ws);
+    if (ws.aborted) stream_drain(sm, ws, w);
 }
 
-template <int R, bool BF16>
-static dflash2_status launch_verify(const ScanGeom &g, const VerifyArgs &a, cudaStream_t stream) {
-    const size_t smem = scan_smem_bytes() + sizeof(DrawScratch);
-    const void *fn = reinterpret_cast<const void *>(&k_verify<R, BF16>);
-    const int per_sm = blocks_per_sm(fn, SCAN_THREADS, smem);
-    int64_t grid = static_cast<int64_t>(sm_count()) * per_sm;
-    if (grid > g.rows) grid = g.rows;
-    k_verify<R, BF16><<<static_cast<unsigned>(grid), SCAN_THREADS, smem, stream>>>(g, a);
+template <bool SAMPLED, bool BF16>
+static dflash2_status launch_verify(const ScanGeom &g, const ScanWs &sw, const VerifyArgs &a,
+                                    cudaStream_t stream) {
+    const size_t smem = scan_smem_bytes();
+    const void *fn = reinterpret_cast<const void *>(&k_verify<SAMPLED, BF16>);
+    const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.total);
+    k_verify<SAMPLED, BF16><<<static_cast<unsigned>(grid), SCAN_THREADS, smem, stream>>>(g, sw, a);
     return after_launch();
 }
 
@@ -353,9 +380,13 @@ static size_t ticket_bytes(int64_t B) {
 
 using namespace dfl;
 
+static size_t recs_bytes(int64_t B, int32_t K) {
+    return (static_cast<size_t>(B) * (K + 1) * sizeof(TRec) + 255) / 256 * 256;
+}
+
 extern "C" size_t dflash2_verify_workspace_bytes(int64_t B, int32_t K) {
     if (B < 0 || K < 1 || K > DFLASH2_MAX_K) return 0;
-    return ticket_bytes(B) + static_cast<size_t>(B) * (K + 1) * sizeof(TRec);
+    return ticket_bytes(B) + recs_bytes(B, K) + scan_ws_bytes(B * (K + 1));
 }
 
 extern "C" dflash2_status dflash2_verify(const void *tlogits, dflash2_dtype dt, int64_t B, int32_t K,
@@ -377,15 +408,8 @@ extern "C" dflash2_status dflash2_verify(const void *tlogits, dflash2_dtype dt, 
     if (params && (!u_acc || !u_res)) return DFLASH2_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(ws) & 15) != 0) return DFLASH2_ERR_INVALID_ARG;
     if (ws_bytes < dflash2_verify_workspace_bytes(B, K)) return DFLASH2_ERR_WORKSPACE;
-    ScanGeom g;
-    g.base = static_cast<const char *>(tlogits);
-    g.ld_bytes = ld * es;
-    g.V = V;
-    g.rows = B * (K + 1);
-    g.chunks_per_row = static_cast<int>((V * es + CHUNK_BYTES - 1) / CHUNK_BYTES);
-    g.params = params;
-    g.rows_per_param = K + 1;
-    g.target = true;
+    const ScanGeom g = make_geom(tlogits, ld, es, V, B * (K + 1), params, K + 1);
+    const ScanWs sw = scan_ws_at(static_cast<char *>(ws) + ticket_bytes(B) + recs_bytes(B, K), B * (K + 1));
     VerifyArgs a;
     a.path_tok = path_tok;
     a.cand_idx = cand_idx;
@@ -402,6 +426,7 @@ extern "C" dflash2_status dflash2_verify(const void *tlogits, dflash2_dtype dt, 
     a.K = K;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (params == nullptr)
-        return dt == DFLASH2_BF16 ? launch_verify<1, true>(g, a, s) : launch_verify<1, false>(g, a, s);
-    return dt == DFLASH2_BF16 ? launch_verify<2, true>(g, a, s) : launch_verify<2, false>(g, a, s);
+        return dt == DFLASH2_BF16 ? launch_verify<false, true>(g, sw, a, s)
+                                  : launch_verify<false, false>(g, sw, a, s);
+    return dt == DFLASH2_BF16 ? launch_verify<true, true>(g, sw, a, s) : launch_verify<true, false>(g, sw, a, s);
 }

@@ -101,12 +101,17 @@ typedef struct {
  *          greedy rows), so that kept candidates have U = z / T' - lse.
  * A row holding a NaN or +Inf, or nothing above -Inf, or with invalid or
  * unsupported parameters, gets cand_idx -1, U NaN and lse NaN.
+ * ws: dflash2_topk16_workspace_bytes(rows) bytes (the kernel splits long rows
+ *   over several CTAs and combines the parts there).
  * Errors: INVALID_ARG if a pointer is NULL or misaligned, rows < 0, V < 16,
- * V >= 2^31, ld < V, ld * elem size not a multiple of 16, rows_per_param < 1.
+ * V >= 2^31, ld < V, ld * elem size not a multiple of 16, rows_per_param < 1;
+ * WORKSPACE if ws_bytes is too small.
  */
+size_t dflash2_topk16_workspace_bytes(int64_t rows);
 dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
                               int64_t ld, const dflash2_sampling *params, int64_t rows_per_param,
-                              int32_t *cand_idx, float *cand_U, float *lse, dflash2_stream stream);
+                              int32_t *cand_idx, float *cand_U, float *lse, void *ws,
+                              size_t ws_bytes, dflash2_stream stream);
 
 /*
  * dflash2_ctx_gate -- [P] item 1 "context gate" of the bilinear selector,

@@ -46,17 +46,21 @@ def test_workspace_sizes(lib):
     assert lib.dflash2_verify_workspace_bytes(1, 0) == 0
     assert lib.dflash2_verify_workspace_bytes(1, 16) == 0
     assert lib.dflash2_pair_score_walk_workspace_bytes(64) >= 256
+    assert lib.dflash2_topk16_workspace_bytes(448) >= 448 * 4
+    assert lib.dflash2_topk16_workspace_bytes(-1) == 0
 
 
 def test_argument_checks_fail_before_any_launch(lib):
     bad = 1  # DFLASH2_ERR_INVALID_ARG
     p = ctypes.c_void_p(16)  # never dereferenced: the checks fail first
     # V < 16
-    assert lib.dflash2_topk16(p, 1, 4, 8, 8, None, 1, p, p, p, None) == bad
+    assert lib.dflash2_topk16(p, 1, 4, 8, 8, None, 1, p, p, p, p, 1 << 22, None) == bad
     # ld * 2 bytes not a multiple of 16
-    assert lib.dflash2_topk16(p, 1, 4, 100, 100, None, 1, p, p, p, None) == bad
+    assert lib.dflash2_topk16(p, 1, 4, 100, 100, None, 1, p, p, p, p, 1 << 22, None) == bad
     # rows_per_param < 1
-    assert lib.dflash2_topk16(p, 1, 4, 128, 128, None, 0, p, p, p, None) == bad
+    assert lib.dflash2_topk16(p, 1, 4, 128, 128, None, 0, p, p, p, p, 1 << 22, None) == bad
+    # no workspace
+    assert lib.dflash2_topk16(p, 1, 4, 128, 128, None, 1, p, p, p, None, 1 << 22, None) == bad
     # K outside 1..15
     assert lib.dflash2_verify(p, 1, 2, 16, 128, 128, p, p, p, p, None, None, None, 0, p, p, p, p, 1 << 20,
                               None) == bad
@@ -72,3 +76,4 @@ def test_argument_checks_fail_before_any_launch(lib):
     assert lib.dflash2_conv2tap(p, p, p, p, 1, 2, 3, 10, 3, p, None) == bad
     # workspace too small
     assert lib.dflash2_verify(p, 1, 2, 3, 128, 128, p, p, p, p, None, None, None, 0, p, p, p, p, 16, None) == 4
+    assert lib.dflash2_topk16(p, 1, 4, 128, 128, None, 1, p, p, p, p, 16, None) == 4
