@@ -5,29 +5,37 @@
 // of whole vocabulary rows: a running max / sum of exponentials, an argmax,
 // or the best N keys.
 //
-// Work split.  The rows are cut into 4 KB chunks and the flat chunk sequence
+// Work split.  The rows are cut into 8 KB chunks and the flat chunk sequence
 // (row-major) is split into one contiguous range per CTA, equal to within a
 // chunk, so every CTA streams the same number of bytes whatever the row count.
 // A row that straddles two or more ranges is reduced by each of its CTAs; each
 // writes a partial result to the workspace and the CTA that completes the row
 // (a per-row ticket) combines the parts in CTA order and finishes the row.
 //
-// Streaming.  Chunk j of a CTA's range belongs to warp j mod 8.  Each warp
-// streams its chunks through a private 2-stage shared-memory ring filled by
-// 1-D bulk copies (cp.async.bulk) that complete on per-stage mbarriers; the
-// warp that consumes a stage refills it, so no cross-warp handshake is needed.
+// Streaming.  Chunk j of a CTA's range belongs to streaming warp j mod 4.
+// Each streaming warp streams its chunks through a private 2-stage
+// shared-memory ring filled by 1-D bulk copies (cp.async.bulk) that complete
+// on per-stage mbarriers.  A warp copies an arrived chunk into registers and
+// refills the stage at once, so two of its chunks are always in flight.
 //
-// Per chunk, each lane first takes the maximum of its 64 (bf16) elements with
-// packed bf16x2 maxima, then (for the log normaliser) its sum of 2^((x-m)c).
-// Argmax: only lanes whose maximum beats the warp's best value rescan their
-// elements.  Best N keys: elements below a value floor cannot be among the N
-// best; the floor is the best of (a) the warp's N-th key, (b) a bound taken
-// from the first chunk (the N-th largest lane maximum: at least N elements
-// reach it) and (c) the best floor any warp of the CTA has published for the
-// row.  Elements at or above the floor are appended to a per-warp candidate
-// buffer in shared memory; a full buffer is sorted (bitonic) and merged into
-// the warp's register-resident list, which raises the floor.  At the end of a
-// row the warp results are merged (bitonic networks) into warp 0.
+// Per chunk, each lane takes the maximum of its 128 (bf16) elements with
+// packed bf16x2 maxima and (for the log normaliser) its sum of 2^((x-m)c)
+// with packed f32x2 multiply-adds and adds.  Argmax: only lanes whose maximum
+// beats the warp's best value revisit their elements.  Best N elements: a
+// lane slice (the 8 KB chunk's 128 elements one lane holds) whose maximum
+// reaches the row's value floor is kept as one key (its maximum, its first
+// element); at least N elements reach the floor, which is the best of the
+// N-th largest lane maximum of the warps' first chunks (taken together
+// behind a named barrier), the warp's own N-th slice key and the best floor
+// the CTA's warps have published for the row.  The N best elements of a row
+// then lie in the slices whose maximum reaches the N-th largest slice maximum
+// F, and are ranked exactly from those slices alone at the end of the row.
+//
+// Row ends.  The streaming warps hand each row's partial results (sorted
+// slice lists, sums, argmax keys) to the CTA's completion warp through
+// double-buffered shared slots and stream on; the completion warp merges
+// them, joins the CTAs of a split row, ranks the row's elements and writes
+// the outputs, and clears the row's shared state before it frees the slot.
 //
 // Waits are bounded: a warp that times out raises the error word, stops
 // issuing copies, waits a bounded time for those in flight and flags its rows.
@@ -37,10 +45,11 @@
 
 namespace dfl {
 
-constexpr int CHUNK_BYTES = 4096;
+constexpr int CHUNK_BYTES = 8192;
 constexpr int WSTAGES = 2;
-constexpr int SCAN_WARPS = 8;
-constexpr int SCAN_THREADS = SCAN_WARPS * 32;
+constexpr int SCAN_WARPS = 4;
+constexpr int SCAN_THREADS = SCAN_WARPS * 32 + 32;  // + one completion warp
+constexpr int STREAM_THREADS = SCAN_WARPS * 32;
 constexpr int VEC_PER_CHUNK = CHUNK_BYTES / 16;
 constexpr int VEC_PER_LANE = VEC_PER_CHUNK / 32;
 constexpr int CAND_CAP = 64;          // candidate buffer of a warp (keys)
@@ -113,14 +122,18 @@ __device__ __forceinline__ int64_t range_owner(const ScanGeom &g, int64_t f) {
 
 struct ScanSmem {
     uint64_t full[SCAN_WARPS][WSTAGES];
-    unsigned int floor_ord[2];  // CTA-wide value floor of the row (ordered bits), by row parity
-    int bad[2];
-    float wm[SCAN_WARPS];
-    float wsum[SCAN_WARPS];
-    uint64_t wbest[SCAN_WARPS];
-    uint32_t lmax[SCAN_WARPS][32];  // sorted lane maxima of each warp's first chunk of the row (ordered bits)
-    uint64_t cand[SCAN_WARPS][CAND_CAP];
-    uint64_t lists[SCAN_WARPS][DFLASH2_MAX_TOPK];
+    uint64_t slot_full[2], slot_empty[2];  // row hand-off (count SCAN_WARPS / 1)
+    unsigned int floor_ord[2];             // CTA-wide value floor of a row (ordered bits), by row parity
+    uint32_t lmax[2][SCAN_WARPS][32];      // sorted lane maxima of each warp's first chunk of a row
+    uint64_t cand[SCAN_WARPS][CAND_CAP];     // slice-key buffers (empty between rows)
+    // Row results handed from the streaming warps to the completion warp.
+    struct Hand {
+        uint64_t lists[SCAN_WARPS][DFLASH2_MAX_TOPK];
+        uint64_t wbest[SCAN_WARPS];
+        float wm[SCAN_WARPS], wsum[SCAN_WARPS];
+        int bad[SCAN_WARPS];
+    } hand[2];
+    unsigned char scratch[1024];  // the completion warp's scratch (gathered keys, verify's draws)
     alignas(128) unsigned char buf[SCAN_WARPS][WSTAGES][CHUNK_BYTES];
 };
 
@@ -214,24 +227,42 @@ __device__ __forceinline__ uint64_t tail_key(float x, uint32_t idx) {
 __device__ __forceinline__ bool key_is_slice(uint64_t k) { return (static_cast<uint32_t>(k) & 0x80000000u) != 0; }
 __device__ __forceinline__ uint32_t key_base(uint64_t k) { return ~static_cast<uint32_t>(k) & 0x7fffffffu; }
 
+// The eight partial sums of the log normaliser (f32x2 pairs).
+__device__ __forceinline__ void scale_sums(uint64_t (&acc)[4], float sc) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        acc[j] = pack2(__float_as_uint(__uint_as_float(lo32(acc[j])) * sc),
+                       __float_as_uint(__uint_as_float(hi32(acc[j])) * sc));
+}
+__device__ __forceinline__ float sum_sums(const uint64_t (&acc)[4]) {
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s += __uint_as_float(lo32(acc[j])) + __uint_as_float(hi32(acc[j]));
+    return s;
+}
+
 template <int R>
 struct ScanState {
     float bv;   // argmax: this lane's best value and its id
     int32_t bi;
     float bw;   // argmax: the warp's best value (warp-uniform)
-    float m, s0, s1, negmc, c;
-    float tau_val;  // value of the warp's N-th slice key (-inf while the list is short); warp-uniform
-    float lo;       // value floor: at least N elements of the row reach it; warp-uniform
-    int nbuf;       // keys in the warp's candidate buffer
+    float m, negmc, c;
+    uint64_t acc[4];  // sum of 2^((x - m) c): eight partial sums as f32x2 pairs
+    float tau_val;    // value of the warp's N-th slice key (-inf while the list is short); warp-uniform
+    float lo;         // value floor: at least N elements of the row reach it; warp-uniform
+    int nbuf;         // keys in the warp's slice buffer
     bool bad;
     WarpList<R> list;  // best slice keys of the warp
 };
 
+// A chunk's 16-byte vectors as one lane holds them in registers: vector q is
+// lane + 32 q; vectors past the chunk's data hold -inf.
 template <bool BF16>
 struct VecLoad;
 template <>
 struct VecLoad<true> {
     static constexpr int VE = 8;
+    static constexpr uint32_t NEG_WORD = 0xff80ff80u;  // two bf16 -inf
     __device__ __forceinline__ static void unpack(uint4 w, float (&x)[8]) {
         x[0] = bf16lo(w.x);
         x[1] = bf16hi(w.x);
@@ -242,49 +273,40 @@ struct VecLoad<true> {
         x[6] = bf16lo(w.w);
         x[7] = bf16hi(w.w);
     }
-    // NaN-propagating maximum of the 8 values of a 16-byte vector.
-    __device__ __forceinline__ static float vmax(const unsigned char *p) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(p);
+    // NaN-propagating maximum of a vector.
+    __device__ __forceinline__ static float vmax(uint4 w) {
         const uint32_t mm = bmax2_nan(bmax2_nan(w.x, w.y), bmax2_nan(w.z, w.w));
         return fmax_nan(bf16lo(mm), bf16hi(mm));
     }
-    // NaN-propagating maximum of this lane's slice (vectors q < nq), packed
-    // bf16x2 maxima; -inf when nq == 0.
-    __device__ __forceinline__ static float lane_max(const unsigned char *tile, int lane, int nq) {
-        uint32_t a = 0xff80ff80u, b = 0xff80ff80u, c = 0xff80ff80u, d = 0xff80ff80u;
-        if (nq == VEC_PER_LANE) {
+    // NaN-propagating maximum of the lane's vectors (packed bf16x2 maxima).
+    __device__ __forceinline__ static float lane_max(const uint4 (&v)[VEC_PER_LANE]) {
+        uint32_t a[8];
 #pragma unroll
-            for (int q = 0; q < VEC_PER_LANE; ++q) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(tile + (lane + q * 32) * 16);
-                a = bmax2_nan(a, w.x);
-                b = bmax2_nan(b, w.y);
-                c = bmax2_nan(c, w.z);
-                d = bmax2_nan(d, w.w);
-            }
-        } else {
-            for (int q = 0; q < nq; ++q) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(tile + (lane + q * 32) * 16);
-                a = bmax2_nan(a, w.x);
-                b = bmax2_nan(b, w.y);
-                c = bmax2_nan(c, w.z);
-                d = bmax2_nan(d, w.w);
-            }
+        for (int j = 0; j < 8; ++j) a[j] = NEG_WORD;
+#pragma unroll
+        for (int q = 0; q < VEC_PER_LANE; ++q) {
+            const int h = (q & 1) * 4;
+            a[h + 0] = bmax2_nan(a[h + 0], v[q].x);
+            a[h + 1] = bmax2_nan(a[h + 1], v[q].y);
+            a[h + 2] = bmax2_nan(a[h + 2], v[q].z);
+            a[h + 3] = bmax2_nan(a[h + 3], v[q].w);
         }
-        const uint32_t mm = bmax2_nan(bmax2_nan(a, b), bmax2_nan(c, d));
+        const uint32_t mm = bmax2_nan(bmax2_nan(bmax2_nan(a[0], a[1]), bmax2_nan(a[2], a[3])),
+                                      bmax2_nan(bmax2_nan(a[4], a[5]), bmax2_nan(a[6], a[7])));
         return fmax_nan(bf16lo(mm), bf16hi(mm));
     }
-    // s0 += 2^(x c + negmc) over the even elements, s1 over the odd ones.
-    __device__ __forceinline__ static void accumulate(const unsigned char *p, float c, float negmc, float &s0,
-                                                      float &s1) {
-        const uint4 w = *reinterpret_cast<const uint4 *>(p);
-        s0 += ex2(fmaf(bf16lo(w.x), c, negmc));
-        s1 += ex2(fmaf(bf16hi(w.x), c, negmc));
-        s0 += ex2(fmaf(bf16lo(w.y), c, negmc));
-        s1 += ex2(fmaf(bf16hi(w.y), c, negmc));
-        s0 += ex2(fmaf(bf16lo(w.z), c, negmc));
-        s1 += ex2(fmaf(bf16hi(w.z), c, negmc));
-        s0 += ex2(fmaf(bf16lo(w.w), c, negmc));
-        s1 += ex2(fmaf(bf16hi(w.w), c, negmc));
+    // acc[j] += (2^(lo_j c + negmc), 2^(hi_j c + negmc)) for the bf16 pair in
+    // word j of the vector (packed f32x2 arithmetic; cc, nn hold c and negmc
+    // in both halves).
+    __device__ __forceinline__ static void accumulate(uint4 w, uint64_t cc, uint64_t nn, uint64_t (&acc)[4]) {
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint64_t x = pack2(ws[j] << 16, ws[j] & 0xffff0000u);
+            const uint64_t t = fma2(x, cc, nn);
+            acc[j] = add2(acc[j], pack2(__float_as_uint(ex2(__uint_as_float(lo32(t)))),
+                                        __float_as_uint(ex2(__uint_as_float(hi32(t))))));
+        }
     }
     __device__ __forceinline__ static float scalar(const char *row, int64_t i) {
         const unsigned short b = reinterpret_cast<const unsigned short *>(row)[i];
@@ -294,41 +316,29 @@ struct VecLoad<true> {
 template <>
 struct VecLoad<false> {
     static constexpr int VE = 4;
+    static constexpr uint32_t NEG_WORD = 0xff800000u;  // f32 -inf
     __device__ __forceinline__ static void unpack(uint4 w, float (&x)[4]) {
         x[0] = __uint_as_float(w.x);
         x[1] = __uint_as_float(w.y);
         x[2] = __uint_as_float(w.z);
         x[3] = __uint_as_float(w.w);
     }
-    __device__ __forceinline__ static float vmax(const unsigned char *p) {
-        const float4 f = *reinterpret_cast<const float4 *>(p);
-        return fmax_nan(fmax_nan(f.x, f.y), fmax_nan(f.z, f.w));
+    __device__ __forceinline__ static float vmax(uint4 w) {
+        return fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
+                        fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
     }
-    __device__ __forceinline__ static float lane_max(const unsigned char *tile, int lane, int nq) {
-        float a = NEG_INF, b = NEG_INF;
-        if (nq == VEC_PER_LANE) {
+    __device__ __forceinline__ static float lane_max(const uint4 (&v)[VEC_PER_LANE]) {
+        float a[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
-            for (int q = 0; q < VEC_PER_LANE; ++q) {
-                const float4 f = *reinterpret_cast<const float4 *>(tile + (lane + q * 32) * 16);
-                a = fmax_nan(a, fmax_nan(f.x, f.y));
-                b = fmax_nan(b, fmax_nan(f.z, f.w));
-            }
-        } else {
-            for (int q = 0; q < nq; ++q) {
-                const float4 f = *reinterpret_cast<const float4 *>(tile + (lane + q * 32) * 16);
-                a = fmax_nan(a, fmax_nan(f.x, f.y));
-                b = fmax_nan(b, fmax_nan(f.z, f.w));
-            }
-        }
-        return fmax_nan(a, b);
+        for (int q = 0; q < VEC_PER_LANE; ++q) a[q & 3] = fmax_nan(a[q & 3], vmax(v[q]));
+        return fmax_nan(fmax_nan(a[0], a[1]), fmax_nan(a[2], a[3]));
     }
-    __device__ __forceinline__ static void accumulate(const unsigned char *p, float c, float negmc, float &s0,
-                                                      float &s1) {
-        const float4 f = *reinterpret_cast<const float4 *>(p);
-        s0 += ex2(fmaf(f.x, c, negmc));
-        s1 += ex2(fmaf(f.y, c, negmc));
-        s0 += ex2(fmaf(f.z, c, negmc));
-        s1 += ex2(fmaf(f.w, c, negmc));
+    __device__ __forceinline__ static void accumulate(uint4 w, uint64_t cc, uint64_t nn, uint64_t (&acc)[4]) {
+        const uint64_t t0 = fma2(pack2(w.x, w.y), cc, nn), t1 = fma2(pack2(w.z, w.w), cc, nn);
+        acc[0] = add2(acc[0], pack2(__float_as_uint(ex2(__uint_as_float(lo32(t0)))),
+                                    __float_as_uint(ex2(__uint_as_float(hi32(t0))))));
+        acc[1] = add2(acc[1], pack2(__float_as_uint(ex2(__uint_as_float(lo32(t1)))),
+                                    __float_as_uint(ex2(__uint_as_float(hi32(t1))))));
     }
     __device__ __forceinline__ static float scalar(const char *row, int64_t i) {
         return reinterpret_cast<const float *>(row)[i];
@@ -364,10 +374,25 @@ __device__ __forceinline__ uint32_t warp_merge_desc_u32(uint32_t a, uint32_t b, 
     return v;
 }
 
-// Named barrier 1 over the first `threads` threads that reach it (a multiple
-// of 32); barrier 0 is __syncthreads.
-__device__ __forceinline__ void named_barrier(int threads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+// Named barrier 1 (even rows of a CTA) or 3 (odd rows) over the first
+// `threads` threads that reach it (a multiple of 32).  Alternating the id
+// keeps the barriers of consecutive rows apart: a warp starts row r + 2 only
+// after the completion warp took row r, i.e. after every warp left row r's
+// barrier.
+__device__ __forceinline__ void row_barrier(int parity, int threads) {
+    if (parity == 0)
+        asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
+    else
+        asm volatile("bar.sync 3, %0;" ::"r"(threads) : "memory");
+}
+
+__device__ __forceinline__ int warp_inclusive_scan_i(int v, int lane) {
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int t = __shfl_up_sync(FULL, v, d);
+        if (lane >= d) v += t;
+    }
+    return v;
 }
 
 // Publish a value floor for the row to the other warps of the CTA.
@@ -375,20 +400,26 @@ __device__ __forceinline__ void publish_floor(ScanSmem &sm, int rp, float v, int
     if (lane == 0 && v > NEG_INF) atomicMax(&sm.floor_ord[rp], f2ord(v));
 }
 
-// Sort the candidate buffer into the list (32 keys at a time) and raise the
-// warp's floor to the value of its N-th slice key.
+// Sort `n` keys of a buffer into the list (32 keys at a time).  Warp-uniform.
 template <int R>
-__device__ __forceinline__ void flush_candidates(ScanSmem &sm, ScanState<R> &st, const uint64_t *cand, int nsel,
-                                                 int lane, int rp) {
-    __syncwarp();
-    for (int base = 0; base < st.nbuf; base += 32) {
-        const uint64_t k = base + lane < st.nbuf ? cand[base + lane] : 0;
+__device__ __forceinline__ void merge_buffer(WarpList<R> &list, const uint64_t *buf, int n, int lane) {
+    for (int base = 0; base < n; base += 32) {
+        const uint64_t k = base + lane < n ? buf[base + lane] : 0;
         WarpList<R> o;
         o.k[0] = warp_sort_desc(k, lane);
 #pragma unroll
         for (int r = 1; r < R; ++r) o.k[r] = 0;
-        st.list.merge(o, lane);
+        list.merge(o, lane);
     }
+}
+
+// Sort the slice buffer into the warp's list and raise the warp's floor to
+// the value of its N-th slice key.
+template <int R>
+__device__ __forceinline__ void flush_candidates(ScanSmem &sm, ScanState<R> &st, const uint64_t *cand, int nsel,
+                                                 int lane, int rp) {
+    __syncwarp();
+    merge_buffer<R>(st.list, cand, st.nbuf, lane);
     st.nbuf = 0;
     __syncwarp();
     const uint64_t tw = st.list.at(nsel - 1);
@@ -428,12 +459,13 @@ __device__ __forceinline__ void scan_one(ScanState<R> &st, float x, uint32_t idx
     }
     if (MODE == MODE_TOPN_LSE && valid) {
         if (x > st.m) {
-            st.s0 *= ex2((st.m - x) * st.c);
-            st.s1 *= ex2((st.m - x) * st.c);
+            scale_sums(st.acc, ex2((st.m - x) * st.c));
             st.m = x;
             st.negmc = -x * st.c;
         }
-        if (st.m != NEG_INF) st.s0 += ex2(fmaf(x, st.c, st.negmc));
+        if (st.m != NEG_INF)
+            st.acc[0] = pack2(__float_as_uint(__uint_as_float(lo32(st.acc[0])) + ex2(fmaf(x, st.c, st.negmc))),
+                              hi32(st.acc[0]));
     }
     const bool c = valid && x == x && x >= fmaxf(st.lo, st.tau_val);
     const uint32_t msk = __ballot_sync(FULL, c);
@@ -447,28 +479,29 @@ __device__ __forceinline__ void scan_one(ScanState<R> &st, float x, uint32_t idx
 // the row publishes the sorted maxima of its lanes, waits for the others
 // (named barrier over the row's `expect` warps, w0 the first of them) and
 // merges their lists: at least N elements reach the N-th largest of those
-// maxima, a floor from 8 chunks instead of one.  A warp whose chunk did not
+// maxima, a floor from 4 chunks instead of one.  A warp whose chunk did not
 // arrive takes part with -inf maxima, so the barrier always completes.
 __device__ __forceinline__ void cta_first_floor(ScanSmem &sm, float &lo, float cmax, int nsel, int expect, int w0,
-                                                int w, int lane) {
+                                                int rp, int w, int lane) {
     uint32_t o = f2ord(cmax == cmax ? cmax : NEG_INF);
     o = warp_sort_desc(o, lane);
-    sm.lmax[w][lane] = o;
-    named_barrier(expect * 32);
+    sm.lmax[rp][w][lane] = o;
+    row_barrier(rp, expect * 32);
 #pragma unroll 1
     for (int i = 0; i < expect; ++i) {
         const int u = (w0 + i) % SCAN_WARPS;
-        if (u != w) o = warp_merge_desc_u32(o, sm.lmax[u][lane], lane);
+        if (u != w) o = warp_merge_desc_u32(o, sm.lmax[rp][u][lane], lane);
     }
     const float f = ord2f(__shfl_sync(FULL, o, nsel - 1));
     lo = fmaxf(lo, f);
 }
 
-// One chunk of a row after its lane maxima (`cmax`, `nq` vectors per lane):
-// `bulk` bytes at `tile`, first element e0.  Warp-uniform.
+// One chunk of a row held in registers (`v`, lane maximum `cmax`), first
+// element e0.  Warp-uniform.
 template <int R, int MODE, bool BF16>
-__device__ __forceinline__ void consume_chunk(ScanSmem &sm, ScanState<R> &st, const unsigned char *tile, int nq,
-                                              float cmax, uint32_t e0, int nsel, int w, int lane, int rp) {
+__device__ __forceinline__ void consume_chunk(ScanSmem &sm, ScanState<R> &st, const uint4 (&v)[VEC_PER_LANE],
+                                              bool has_data, float cmax, uint32_t e0, int nsel, int w, int lane,
+                                              int rp) {
     using VL = VecLoad<BF16>;
     constexpr int VE = VL::VE;
     if (cmax != cmax) st.bad = true;
@@ -476,17 +509,17 @@ __device__ __forceinline__ void consume_chunk(ScanSmem &sm, ScanState<R> &st, co
         const bool f = cmax > st.bw;
         if (f) {  // rare after the first chunks: the lane's new best, in index order
             float t = st.bw;
-            for (int q = 0; q < nq; ++q) {
-                const int v = lane + q * 32;
-                if (VL::vmax(tile + v * 16) > t) {
+#pragma unroll
+            for (int q = 0; q < VEC_PER_LANE; ++q) {
+                if (VL::vmax(v[q]) > t) {
                     float x[VE];
-                    VL::unpack(*reinterpret_cast<const uint4 *>(tile + v * 16), x);
+                    VL::unpack(v[q], x);
 #pragma unroll
                     for (int e = 0; e < VE; ++e) {
                         if (x[e] > t) {
                             t = x[e];
                             st.bv = x[e];
-                            st.bi = static_cast<int32_t>(e0 + v * VE + e);
+                            st.bi = static_cast<int32_t>(e0 + (lane + q * 32) * VE + e);
                         }
                     }
                 }
@@ -497,60 +530,85 @@ __device__ __forceinline__ void consume_chunk(ScanSmem &sm, ScanState<R> &st, co
     }
     if (MODE == MODE_TOPN_LSE) {
         if (cmax > st.m) {  // rare after the first chunks: rescale once per chunk
-            const float sc = ex2((st.m - cmax) * st.c);
-            st.s0 *= sc;
-            st.s1 *= sc;
+            scale_sums(st.acc, ex2((st.m - cmax) * st.c));
             st.m = cmax;
             st.negmc = -cmax * st.c;
         }
         if (st.m != NEG_INF) {
-            if (nq == VEC_PER_LANE) {
-#pragma unroll 4
-                for (int q = 0; q < VEC_PER_LANE; ++q)
-                    VL::accumulate(tile + (lane + q * 32) * 16, st.c, st.negmc, st.s0, st.s1);
-            } else {
-                for (int q = 0; q < nq; ++q)
-                    VL::accumulate(tile + (lane + q * 32) * 16, st.c, st.negmc, st.s0, st.s1);
-            }
+            const uint64_t cc = pack2(__float_as_uint(st.c), __float_as_uint(st.c));
+            const uint64_t nn = pack2(__float_as_uint(st.negmc), __float_as_uint(st.negmc));
+#pragma unroll
+            for (int q = 0; q < VEC_PER_LANE; ++q) VL::accumulate(v[q], cc, nn, st.acc);
         }
     }
     // The CTA's floor for the row (one read, broadcast).
     uint32_t so = lane == 0 ? *reinterpret_cast<volatile unsigned int *>(&sm.floor_ord[rp]) : 0u;
     so = __shfl_sync(FULL, so, 0);
     if (so != 0) st.lo = fmaxf(st.lo, ord2f(so));
-    const bool lf = nq > 0 && cmax >= fmaxf(st.lo, st.tau_val);
+    const bool lf = has_data && cmax >= fmaxf(st.lo, st.tau_val);
     if (__any_sync(FULL, lf))
         take_slices<R>(sm, st, lf, cmax, slice_key(cmax, e0 + lane * VE), nsel, lane, sm.cand[w], rp);
 }
 
 __device__ __forceinline__ bool row_streams(const RowTask &t) { return t.mode != MODE_SKIP; }
 
-// Consume the warp's chunks of the CTA's row `rrel` (global row `row`) and
-// merge the warps; on return warp 0 holds the CTA's result for the row (best
-// slice keys for modes TOPN*).  Every row of the range goes through here
-// (rows that need no scan with `skip`), so that the chunk streams stay in
-// step.  `rp` is the parity of the row within the CTA's rows; `expect` warps,
-// from warp w0 on (cyclically), hold a chunk of it.
+// A streaming warp's results for the row into hand-off slot rp; the warp's
+// arrival on slot_full[rp] (count SCAN_WARPS) publishes them.
+template <int R>
+__device__ __forceinline__ void hand_off_warp(ScanSmem &sm, int rp, int w, int lane, const ScanState<R> &st) {
+    ScanSmem::Hand &h = sm.hand[rp];
+    const uint64_t kb = warp_max_u64(st.bi >= 0 ? make_key(st.bv, static_cast<uint32_t>(st.bi)) : 0);
+    float mm = st.m, s = sum_sums(st.acc);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const float m2 = __shfl_xor_sync(FULL, mm, d);
+        const float s2 = __shfl_xor_sync(FULL, s, d);
+        lse_combine(mm, s, m2, s2, st.c);
+    }
+    const bool bad = __any_sync(FULL, st.bad);
+    st.list.store(h.lists[w], lane);
+    if (lane == 0) {
+        h.wbest[w] = kb;
+        h.wm[w] = mm;
+        h.wsum[w] = s;
+        h.bad[w] = bad ? 1 : 0;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.slot_full[rp]);
+}
+
+// A streaming warp's part of the CTA's row `rrel` (global row `row`):
+// consume the warp's chunks of it and hand the warp's partial results to the
+// completion warp.  Every row of the range goes through here (rows that need
+// no scan with `skip`), so that the chunk streams stay in step.  `expect`
+// warps, from warp w0 on (cyclically), hold a chunk of the row.
 template <int R, int MODE, bool BF16>
 __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, const RowTask &task,
-                                         int64_t row, int rrel, int rp, int expect, int w0, bool skip,
-                                         RowResult<R> &res, unsigned int *err_word) {
+                                         int64_t row, int rrel, int expect, int w0, bool skip,
+                                         unsigned int *err_word) {
     using VL = VecLoad<BF16>;
     constexpr int esz = BF16 ? 2 : 4;
     constexpr int CE = CHUNK_BYTES / esz;
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     const int nsel = task.nsel;
+    const int rp = rrel & 1;
+
+    // Slot rp (buffers, lists, floor) is free once row rrel - 2 was taken.
+    bool slot_ok = true;
+    if (rrel >= 2) slot_ok = __all_sync(FULL, mbar_wait(&sm.slot_empty[rp], ((rrel >> 1) - 1) & 1, WAIT_CYCLES));
+    if (!slot_ok && lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
 
     ScanState<R> st;
     st.bv = NEG_INF;
     st.bi = -1;
     st.bw = NEG_INF;
     st.m = NEG_INF;
-    st.s0 = st.s1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) st.acc[j] = 0;
     st.negmc = 0.0f;
     st.c = LOG2E / task.T;
-    st.bad = false;
+    st.bad = !slot_ok;
     st.list.clear();
     st.tau_val = NEG_INF;
     st.lo = NEG_INF;
@@ -567,20 +625,30 @@ __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpSt
         }
         if (!ok) st.bad = true;
         const int c = ws.cons_c;
-        const unsigned char *tile = sm.buf[w][stage];
         const int bulk = static_cast<int>(chunk_bulk_bytes(g, c));
-        int nq = VEC_PER_LANE;
-        if (bulk != CHUNK_BYTES) {
-            const int nvt = bulk >> 4;  // valid vectors in the chunk
-            nq = nvt > lane ? (nvt - lane + 31) >> 5 : 0;
+        const int nvt = bulk >> 4;  // vectors in the chunk
+        const bool compute = ok && !skip;
+        // Copy the lane's vectors into registers, then refill the stage.
+        uint4 v[VEC_PER_LANE];
+        const unsigned char *tile = sm.buf[w][stage];
+#pragma unroll
+        for (int q = 0; q < VEC_PER_LANE; ++q) {
+            const int vi = lane + q * 32;
+            v[q] = (compute && vi < nvt) ? *reinterpret_cast<const uint4 *>(tile + vi * 16)
+                                         : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+        }
+        __syncwarp();
+        if (ok) {
+            ++ws.cons_k;
+            if (ws.iss_k < ws.n_w) stream_issue(sm, g, ws, w, lane);
         }
         float cmax = NEG_INF;
-        if (ok && !skip) cmax = VL::lane_max(tile, lane, nq);
+        if (compute) cmax = VL::lane_max(v);
         if (MODE != MODE_ARGMAX && first && !skip && nsel <= 32 && expect > 1)
-            cta_first_floor(sm, st.lo, cmax, nsel, expect, w0, w, lane);
-        if (ok && !skip) {
+            cta_first_floor(sm, st.lo, cmax, nsel, expect, w0, rp, w, lane);
+        if (compute) {
             const uint32_t e0 = static_cast<uint32_t>(c) * CE;
-            consume_chunk<R, MODE, BF16>(sm, st, tile, nq, cmax, e0, nsel, w, lane, rp);
+            consume_chunk<R, MODE, BF16>(sm, st, v, lane < nvt, cmax, e0, nsel, w, lane, rp);
             // Ragged end of the row (fewer than 16 bytes), read by lane 0.
             if (c == g.cpr - 1) {
                 const char *rbase = g.base + row * g.ld_bytes;
@@ -592,87 +660,25 @@ __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpSt
             }
         }
         first = false;
-        __syncwarp();
         // After a time-out nothing more is issued or waited for (cons_k stays
         // behind iss_k for the drain); the position still advances.
-        if (ok) {
-            ++ws.cons_k;
-            // Refill this stage with the chunk WSTAGES ahead (possibly of a later row).
-            if (ws.iss_k < ws.n_w) stream_issue(sm, g, ws, w, lane);
-        }
         ws.cons_c += SCAN_WARPS;
         while (ws.cons_c >= g.cpr) {
             ws.cons_c -= g.cpr;
             ++ws.cons_r;
         }
     }
-    if (MODE != MODE_ARGMAX && st.nbuf > 0) flush_candidates<R>(sm, st, sm.cand[w], nsel, lane, rp);
 
-    // ---- merge the warps' results into warp 0 ----
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        sm.floor_ord[rp ^ 1] = 0;
-        sm.bad[rp ^ 1] = 0;
-    }
-    if (__any_sync(FULL, st.bad) && lane == 0) sm.bad[rp] = 1;
-    if (MODE == MODE_ARGMAX) {
-        uint64_t kb = st.bi >= 0 ? make_key(st.bv, static_cast<uint32_t>(st.bi)) : 0;
-        kb = warp_max_u64(kb);
-        if (lane == 0) sm.wbest[w] = kb;
-    } else {
-        if (MODE == MODE_TOPN_LSE) {
-            float mm = st.m, s = st.s0 + st.s1;
-#pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) {
-                const float m2 = __shfl_xor_sync(FULL, mm, d);
-                const float s2 = __shfl_xor_sync(FULL, s, d);
-                lse_combine(mm, s, m2, s2, st.c);
-            }
-            if (lane == 0) {
-                sm.wm[w] = mm;
-                sm.wsum[w] = s;
-            }
-        }
-        st.list.store(sm.lists[w], lane);
-    }
-    __syncthreads();
-    if (MODE != MODE_ARGMAX) {
-#pragma unroll
-        for (int stride = 1; stride < SCAN_WARPS; stride *= 2) {
-            if ((w % (2 * stride)) == 0) {
-                WarpList<R> o;
-                o.load(sm.lists[w + stride], lane);
-                st.list.merge(o, lane);
-                if (2 * stride < SCAN_WARPS) st.list.store(sm.lists[w], lane);
-            }
-            if (2 * stride < SCAN_WARPS) __syncthreads();
-        }
-    }
-    if (w == 0) {
-        res.bad = sm.bad[rp] != 0;
-        res.list = st.list;
-        res.best = 0;
-        res.m = NEG_INF;
-        res.s = 0.0f;
-        if (MODE == MODE_ARGMAX) {
-            uint64_t b = 0;
-            for (int i = 0; i < SCAN_WARPS; ++i) b = sm.wbest[i] > b ? sm.wbest[i] : b;
-            res.best = b;
-        }
-        if (MODE == MODE_TOPN_LSE) {
-            float mm = sm.wm[0], s = sm.wsum[0];
-            for (int i = 1; i < SCAN_WARPS; ++i) lse_combine(mm, s, sm.wm[i], sm.wsum[i], st.c);
-            res.m = mm;
-            res.s = s;
-        }
-    }
-    // The next row's merge overwrites sm.lists and the per-warp slots only
-    // after its own first barrier, which warp 0 reaches after reading here.
+    // ---- sort the slice buffer into the list; hand the warp's part of the
+    // row to the completion warp ----
+    if (MODE != MODE_ARGMAX && st.nbuf > 0) flush_candidates<R>(sm, st, sm.cand[w], nsel, lane, rp);
+    hand_off_warp(sm, rp, w, lane, st);
 }
 
 // Offer every element of the slices chosen by this warp's lanes (`take`,
 // slice or tail key `k`) that reaches `F` to the element list `out`, one
-// element per lane at a time; `otau` is out's N-th key.  Warp-uniform.
+// element per lane at a time; `otau` is out's N-th key.  A slice is visited
+// in groups of vectors of 64 elements.  Warp-uniform.
 template <int R, bool BF16>
 __device__ __forceinline__ void offer_slices(const ScanGeom &g, const char *rowp, bool take, uint64_t k, float F,
                                              int nsel, int lane, WarpList<R> &out, uint64_t &otau) {
@@ -680,65 +686,118 @@ __device__ __forceinline__ void offer_slices(const ScanGeom &g, const char *rowp
     constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
     constexpr int CE = CHUNK_BYTES / esz;
-    uint64_t cm = 0;
-    uint32_t base = key_base(k);
+    constexpr int GV = 64 / VE;                 // vectors per group
+    constexpr int NG = VEC_PER_LANE / GV;       // groups per slice
+    static_assert(NG * GV == VEC_PER_LANE, "slices split into whole groups");
+    const uint32_t base = key_base(k);
     const bool slice = key_is_slice(k);
-    if (take) {
-        if (slice) {
-            const int c = static_cast<int>(base / CE);
-            const int lin = static_cast<int>((base % CE) / VE);
-            const int bulk = static_cast<int>(chunk_bulk_bytes(g, c));
-#pragma unroll
-            for (int q = 0; q < VEC_PER_LANE; ++q) {
-                if ((lin + q * 32) * 16 < bulk) {
-                    const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(rowp + static_cast<int64_t>(base + q * 32 * VE) * esz));
-                    float x[VE];
-                    VL::unpack(v, x);
-#pragma unroll
-                    for (int e = 0; e < VE; ++e)
-                        if (x[e] >= F) cm |= 1ull << (q * VE + e);  // NaN never passes
-                }
-            }
-        } else {
-            cm = 1;
-        }
+    int lin = 0, bulk = 0;
+    if (slice) {
+        const int c = static_cast<int>(base / CE);
+        lin = static_cast<int>((base % CE) / VE);
+        bulk = static_cast<int>(chunk_bulk_bytes(g, c));
     }
-    while (__any_sync(FULL, cm != 0)) {
-        uint64_t key = 0;
-        if (cm) {
-            const int b = __ffsll(static_cast<long long>(cm)) - 1;
-            cm &= cm - 1;
+#pragma unroll 1
+    for (int gi = 0; gi < NG; ++gi) {
+        uint64_t cm = 0;
+        if (take) {
             if (slice) {
-                const uint32_t idx = base + (b / VE) * 32 * VE + (b % VE);
-                key = make_key(VL::scalar(rowp, idx), idx);
-            } else {
-                key = make_key(key_val(k), base);
-            }
-            if (key <= otau) key = 0;
-        }
-        if (__any_sync(FULL, key != 0)) {
-            WarpList<R> o;
-            o.k[0] = warp_sort_desc(key, lane);
 #pragma unroll
-            for (int r = 1; r < R; ++r) o.k[r] = 0;
-            out.merge(o, lane);
-            otau = out.at(nsel - 1);
+                for (int j = 0; j < GV; ++j) {
+                    const int q = gi * GV + j;
+                    if ((lin + q * 32) * 16 < bulk) {
+                        const uint4 v = __ldcg(
+                            reinterpret_cast<const uint4 *>(rowp + static_cast<int64_t>(base + q * 32 * VE) * esz));
+                        float x[VE];
+                        VL::unpack(v, x);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e)
+                            if (x[e] >= F) cm |= 1ull << (j * VE + e);  // NaN never passes
+                    }
+                }
+            } else if (gi == 0) {
+                cm = 1;
+            }
+        }
+        while (__any_sync(FULL, cm != 0)) {
+            uint64_t key = 0;
+            if (cm) {
+                const int b = __ffsll(static_cast<long long>(cm)) - 1;
+                cm &= cm - 1;
+                if (slice) {
+                    const uint32_t idx = base + (gi * GV + b / VE) * 32 * VE + (b % VE);
+                    key = make_key(VL::scalar(rowp, idx), idx);
+                } else {
+                    key = make_key(key_val(k), base);
+                }
+                if (key <= otau) key = 0;
+            }
+            if (__any_sync(FULL, key != 0)) {
+                WarpList<R> o;
+                o.k[0] = warp_sort_desc(key, lane);
+#pragma unroll
+                for (int r = 1; r < R; ++r) o.k[r] = 0;
+                out.merge(o, lane);
+                otau = out.at(nsel - 1);
+            }
         }
     }
 }
 
-// Warp 0, once per row (modes TOPN*): the N best elements of the row from
-// its best slice keys L.  F, the N-th largest slice maximum, is reached by at
-// least N elements, so every one of the N best elements lies in a slice whose
-// maximum reaches F: re-read those slices and rank their elements.  If the
-// list is full with its last key tied at F, slices tied at F may have been
-// left out: then rank every slice of the row.  Returns element keys.
+// Completion warp: the CTA's result for its row rrel (bounded wait for the
+// streaming warps' hand-offs; a time-out marks the row bad and stops further
+// waits), merged over the warps' sorted lists; then clear the row's shared
+// floor and free the slot.
+template <int R, int MODE>
+__device__ __forceinline__ void take_row(ScanSmem &sm, RowResult<R> &res, int rrel, float c, bool &aborted,
+                                         int lane, unsigned int *err_word) {
+    const int rp = rrel & 1;
+    bool ok = !aborted && mbar_wait(&sm.slot_full[rp], (rrel >> 1) & 1, WAIT_CYCLES);
+    ok = __all_sync(FULL, ok);
+    if (!ok && !aborted && lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
+    if (!ok) aborted = true;
+    const ScanSmem::Hand &h = sm.hand[rp];
+    res.list.clear();
+    res.best = 0;
+    res.m = NEG_INF;
+    res.s = 0.0f;
+    res.bad = !ok;
+    if (ok) {
+        for (int u = 0; u < SCAN_WARPS; ++u) {
+            res.bad |= h.bad[u] != 0;
+            if (MODE == MODE_ARGMAX) {
+                res.best = h.wbest[u] > res.best ? h.wbest[u] : res.best;
+            } else {
+                WarpList<R> o;
+                o.load(h.lists[u], lane);
+                res.list.merge(o, lane);
+                if (MODE == MODE_TOPN_LSE) lse_combine(res.m, res.s, h.wm[u], h.wsum[u], c);
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+        sm.floor_ord[rp] = 0;
+        mbar_arrive(&sm.slot_empty[rp]);
+    }
+}
+
+// Completion warp, once per row (modes TOPN*): the N best elements of the row
+// from its best slice keys L.  F, the N-th largest slice maximum, is reached
+// by at least N elements, so every one of the N best elements lies in a slice
+// whose maximum reaches F: re-read those slices, gather their elements that
+// reach F in shared memory and rank them.  If the list is full with its last
+// key tied at F (slices tied at F may have been left out), or the gathered
+// elements overflow the buffer, rank every slice of the row instead.
+// Returns element keys.
 template <int R, bool BF16>
 __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t row, const WarpList<R> &L, int nsel,
-                                                 int lane) {
+                                                    unsigned char *scratch, int lane) {
+    using VL = VecLoad<BF16>;
+    constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
     constexpr int CE = CHUNK_BYTES / esz;
-    using VL = VecLoad<BF16>;
+    constexpr int GCAP = 1024 / 8;
     const char *rowp = g.base + row * g.ld_bytes;
     const uint64_t kN = L.at(nsel - 1);
     const float F = kN ? key_val(kN) : NEG_INF;
@@ -746,16 +805,68 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
     WarpList<R> out;
     out.clear();
     uint64_t otau = 0;
+    uint64_t *gbuf = reinterpret_cast<uint64_t *>(scratch);
     if (!(kL != 0 && key_val(kL) == F)) {
+        // Lane p holds list entry p (p = r*32 + lane) and gathers the
+        // elements of its slice (or its single tail element) that reach F,
+        // half a slice (GV vectors) at a time: all loads of the half first,
+        // then a count, an offset from a warp scan, and the keys.
+        constexpr int GV = VEC_PER_LANE / 2;
+        int total = 0;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const uint64_t k = L.k[r];
-            offer_slices<R, BF16>(g, rowp, k != 0 && key_val(k) >= F, k, F, nsel, lane, out, otau);
+            const bool take = k != 0 && key_val(k) >= F;
+            const uint32_t base = key_base(k);
+            const bool slice = key_is_slice(k);
+            int lin = 0, nvt = 0;
+            if (slice) {
+                const int c = static_cast<int>(base / CE);
+                lin = static_cast<int>((base % CE) / VE);
+                nvt = static_cast<int>(chunk_bulk_bytes(g, c)) >> 4;
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint4 v[GV];
+#pragma unroll
+                for (int j = 0; j < GV; ++j) {
+                    const int q = h * GV + j;
+                    const bool in = take && slice && lin + q * 32 < nvt;
+                    v[j] = make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+                    if (in) v[j] = __ldcg(reinterpret_cast<const uint4 *>(rowp + static_cast<int64_t>(base + q * 32 * VE) * esz));
+                }
+                int cnt = (h == 0 && take && !slice) ? 1 : 0;
+#pragma unroll
+                for (int j = 0; j < GV; ++j) {
+                    float x[VE];
+                    VL::unpack(v[j], x);
+#pragma unroll
+                    for (int e = 0; e < VE; ++e) cnt += x[e] >= F;  // NaN never passes
+                }
+                const int incl = warp_inclusive_scan_i(cnt, lane);
+                int pos = total + incl - cnt;
+                total += __shfl_sync(FULL, incl, 31);
+                if (cnt > 0 && total <= GCAP) {
+                    if (h == 0 && take && !slice) gbuf[pos++] = make_key(key_val(k), base);
+#pragma unroll
+                    for (int j = 0; j < GV; ++j) {
+                        float x[VE];
+                        VL::unpack(v[j], x);
+#pragma unroll
+                        for (int e = 0; e < VE; ++e)
+                            if (x[e] >= F) gbuf[pos++] = make_key(x[e], base + (h * GV + j) * 32 * VE + e);
+                    }
+                }
+            }
         }
-        return out;
+        __syncwarp();
+        if (total <= GCAP) {
+            merge_buffer<R>(out, gbuf, total, lane);
+            return out;
+        }
     }
     for (int c = 0; c < g.cpr; ++c) {
-        const uint32_t base = static_cast<uint32_t>(c) * CE + lane * VL::VE;
+        const uint32_t base = static_cast<uint32_t>(c) * CE + lane * VE;
         const bool take = lane * 16 < static_cast<int>(chunk_bulk_bytes(g, c));
         offer_slices<R, BF16>(g, rowp, take, slice_key(F, base), F, nsel, lane, out, otau);
     }
@@ -793,14 +904,13 @@ __device__ __forceinline__ bool join_parts(const ScanGeom &g, const ScanWs &sw, 
         mine->s = res.s;
         mine->bad = res.bad ? 1 : 0;
     }
-    __threadfence();
     __syncwarp();
     int old = 0;
-    if (lane == 0) old = atomicAdd(&sw.tickets[row], 1);
+    if (lane == 0) old = atomic_add_acq_rel(&sw.tickets[row], 1);
     old = __shfl_sync(FULL, old, 0);
     if (old != static_cast<int>(b1 - b0)) return false;
-    if (lane == 0) sw.tickets[row] = 0;
-    __threadfence();
+    if (lane == 0) sw.tickets[row] = 0;  // zero again for the next call
+    __syncwarp();
     bool bad = false;
     uint64_t best = 0;
     float m = NEG_INF, s = 0.0f;
@@ -833,8 +943,11 @@ __device__ __forceinline__ void scan_init(ScanSmem &sm) {
     if (threadIdx.x == 0) {
         for (int w = 0; w < SCAN_WARPS; ++w)
             for (int s = 0; s < WSTAGES; ++s) mbar_init(&sm.full[w][s], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&sm.slot_full[s], SCAN_WARPS);
+            mbar_init(&sm.slot_empty[s], 1);
+        }
         sm.floor_ord[0] = sm.floor_ord[1] = 0;
-        sm.bad[0] = sm.bad[1] = 0;
         fence_barrier_init();
     }
     __syncthreads();

@@ -55,6 +55,9 @@ __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const Ro
 
 // SAMPLED: some request may sample (params given): lists of 64 keys and every
 // row mode; otherwise every row is greedy (top-16 and the log normaliser).
+// Warps 0..SCAN_WARPS-1 stream the CTA's rows; the last warp completes each
+// row (joins the CTAs of a split row, ranks its elements, writes outputs)
+// while the others stream the next.
 template <bool SAMPLED, bool BF16>
 __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_topk16(ScanGeom g, ScanWs sw,
                                                                                   int32_t *cand_idx,
@@ -67,39 +70,54 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
     const int w = threadIdx.x >> 5;
     scan_init(sm);
     const int64_t begin = range_begin(g, blockIdx.x), end = range_begin(g, blockIdx.x + 1);
-    WarpStream ws;
-    stream_start(sm, g, ws, begin, end, w, lane);
     const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
+    if (w < SCAN_WARPS) {
+        WarpStream ws;
+        stream_start(sm, g, ws, begin, end, w, lane);
+        for (int64_t row = r_first; row <= r_last; ++row) {
+            const int rrel = static_cast<int>(row - r_first);
+            int w0;
+            const int expect = row_warps(g, row, begin, end, &w0);
+            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, false);
+            if (!SAMPLED || task.mode == MODE_TOPN_LSE)
+                scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_topk);
+            else if (task.mode == MODE_TOPN)
+                scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_topk);
+            else
+                scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, expect, w0, true, &g_err_topk);
+        }
+        if (ws.aborted) stream_drain(sm, ws, w);
+        return;
+    }
+    bool aborted = false;
     for (int64_t row = r_first; row <= r_last; ++row) {
-        const int rrel = static_cast<int>(row - r_first), rp = rrel & 1;
-        int w0;
-        const int expect = row_warps(g, row, begin, end, &w0);
+        const int rrel = static_cast<int>(row - r_first);
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, false);
+        const float c = LOG2E / task.T;
         RowResult<R> res;
+        bool done;
         if (!SAMPLED || task.mode == MODE_TOPN_LSE) {
-            scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_topk);
-            if (w == 0 && join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, LOG2E / task.T, lane)) {
-                if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, lane);
-                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
-            }
+            take_row<R, MODE_TOPN_LSE>(sm, res, rrel, c, aborted, lane, &g_err_topk);
+            done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, c, lane);
         } else if (task.mode == MODE_TOPN) {
-            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_topk);
-            if (w == 0 && join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E / task.T, lane)) {
-                if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, lane);
-                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
-            }
+            take_row<R, MODE_TOPN>(sm, res, rrel, c, aborted, lane, &g_err_topk);
+            done = join_parts<R, MODE_TOPN>(g, sw, row, res, c, lane);
         } else {
-            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, true, res, &g_err_topk);
-            if (w == 0 && blockIdx.x == range_owner(g, row * g.cpr)) {
+            take_row<R, MODE_ARGMAX>(sm, res, rrel, c, aborted, lane, &g_err_topk);
+            if (blockIdx.x == range_owner(g, row * g.cpr)) {
                 if (lane < NC) {
                     cand_idx[row * NC + lane] = -1;
                     cand_U[row * NC + lane] = NAN;
                 }
                 if (lane == 0) lse[row] = NAN;
             }
+            continue;
+        }
+        if (done) {
+            if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, lane);
+            finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
         }
     }
-    if (ws.aborted) stream_drain(sm, ws, w);
 }
 
 template <bool SAMPLED, bool BF16>

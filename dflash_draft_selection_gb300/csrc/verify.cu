@@ -89,7 +89,7 @@ struct DrawScratch {
     int32_t sid[DFLASH2_MAX_TOPK];
     float sw[DFLASH2_MAX_TOPK];
 };
-static_assert(sizeof(DrawScratch) <= sizeof(ScanSmem::lists), "the draw scratch lives in the list slots");
+static_assert(sizeof(DrawScratch) <= sizeof(ScanSmem::scratch), "the draw scratch fits the completion warp's scratch");
 
 // Inverse CDF over the entries sorted by ascending token id: the first entry
 // whose running weight exceeds u * (total weight); if rounding leaves none,
@@ -285,20 +285,22 @@ template <bool SAMPLED>
 __device__ void row_done(const VerifyArgs &a, const dflash2_sampling *params, int64_t row,
                          int64_t V, DrawScratch &sc, int lane) {
     const int64_t b = row / (a.K + 1);
-    __threadfence();
     __syncwarp();
     int old = 0;
-    if (lane == 0) old = atomicAdd(&a.tickets[b], 1);
+    if (lane == 0) old = atomic_add_acq_rel(&a.tickets[b], 1);
     old = __shfl_sync(FULL, old, 0);
     if (old == a.K) {
-        if (lane == 0) a.tickets[b] = 0;
-        __threadfence();
+        if (lane == 0) a.tickets[b] = 0;  // zero again for the next call
+        __syncwarp();
         accept_request<SAMPLED>(a, params, b, V, sc, lane);
     }
 }
 
 // SAMPLED: some request may sample (params given); otherwise every row is
-// an argmax and every request greedy.
+// an argmax and every request greedy.  Warps 0..SCAN_WARPS-1 stream the
+// CTA's rows; the last warp completes each row (joins the CTAs of a split
+// row, writes its record and runs the accept walk of a completed request)
+// while the others stream the next.
 template <bool SAMPLED, bool BF16>
 __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_verify(ScanGeom g, ScanWs sw,
                                                                                   VerifyArgs a) {
@@ -307,48 +309,60 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_ve
     unsigned char *base = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(base);
-    // The accept walk runs on warp 0 between two rows, while the per-warp
-    // list slots are idle (they are written again only after the next row's
-    // first barrier, which warp 0 reaches after the walk).
-    DrawScratch &sc = *reinterpret_cast<DrawScratch *>(&sm.lists[0][0]);
+    DrawScratch &sc = *reinterpret_cast<DrawScratch *>(sm.scratch);
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     scan_init(sm);
     const int64_t begin = range_begin(g, blockIdx.x), end = range_begin(g, blockIdx.x + 1);
-    WarpStream ws;
-    stream_start(sm, g, ws, begin, end, w, lane);
     const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
+    if (w < SCAN_WARPS) {
+        WarpStream ws;
+        stream_start(sm, g, ws, begin, end, w, lane);
+        for (int64_t row = r_first; row <= r_last; ++row) {
+            const int rrel = static_cast<int>(row - r_first);
+            int w0;
+            const int expect = row_warps(g, row, begin, end, &w0);
+            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
+            if (!SAMPLED || task.mode == MODE_ARGMAX)
+                scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_verify);
+            else if (task.mode == MODE_TOPN)
+                scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_verify);
+            else
+                scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, expect, w0, true, &g_err_verify);
+        }
+        if (ws.aborted) stream_drain(sm, ws, w);
+        return;
+    }
+    bool aborted = false;
     for (int64_t row = r_first; row <= r_last; ++row) {
-        const int rrel = static_cast<int>(row - r_first), rp = rrel & 1;
-        int w0;
-        const int expect = row_warps(g, row, begin, end, &w0);
+        const int rrel = static_cast<int>(row - r_first);
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
         TRec *rec = a.recs + row;
         RowResult<R> res;
-        bool done = false;
+        bool done;
         if (!SAMPLED || task.mode == MODE_ARGMAX) {
-            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_verify);
-            done = w == 0 && join_parts<R, MODE_ARGMAX>(g, sw, row, res, LOG2E, lane);
+            take_row<R, MODE_ARGMAX>(sm, res, rrel, LOG2E, aborted, lane, &g_err_verify);
+            done = join_parts<R, MODE_ARGMAX>(g, sw, row, res, LOG2E, lane);
         } else if (task.mode == MODE_TOPN) {
-            scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, false, res, &g_err_verify);
-            done = w == 0 && join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
-            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, lane);
+            take_row<R, MODE_TOPN>(sm, res, rrel, LOG2E, aborted, lane, &g_err_verify);
+            done = join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
+            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, lane);
         } else {
-            scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, rp, expect, w0, true, res, &g_err_verify);
-            if (w == 0 && blockIdx.x == range_owner(g, row * g.cpr)) {
+            take_row<R, MODE_ARGMAX>(sm, res, rrel, LOG2E, aborted, lane, &g_err_verify);
+            if (blockIdx.x == range_owner(g, row * g.cpr)) {
                 if (lane == 0) {
                     rec->n = 0;
                     rec->flags = task.status;
                 }
                 row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
             }
+            continue;
         }
         if (done) {
             finalize_target<R>(res, task, rec, lane);
             row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
         }
     }
-    if (ws.aborted) stream_drain(sm, ws, w);
 }
 
 template <bool SAMPLED, bool BF16>
