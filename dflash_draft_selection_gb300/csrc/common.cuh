@@ -94,6 +94,23 @@ __device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
     return old;
 }
 
+// Thread-block clusters.  cluster_sync: all threads of all CTAs of the
+// cluster (release / acquire); the warp reconverges first.
+__device__ __forceinline__ void cluster_sync() {
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Read a float of CTA `rank`'s shared memory at the address of `local` in
+// this CTA (the data is stable between two cluster barriers).
+__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {
+    uint32_t remote;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    float v;
+    asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
+    return v;
+}
+
 // NaN-propagating maxima.
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float d;

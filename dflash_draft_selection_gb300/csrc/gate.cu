@@ -95,25 +95,20 @@ __device__ __forceinline__ void tma_load_2d(void *sdst, const CUtensorMap *tmap,
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_addr(bar)), "r"(x), "r"(y)
         : "memory");
 }
-// Aligned cluster barrier: reconverge the warp first.
-__device__ __forceinline__ void cluster_sync() {
-    __syncwarp();
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
 }
+// Read a float4 of another CTA's shared memory in the cluster.  The data is
+// stable between two cluster barriers, so the loads may be reordered freely.
 __device__ __forceinline__ float4 ld_dsmem_f4(const float *local, uint32_t rank) {
     uint32_t remote;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
     float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(remote)
-                 : "memory");
+    asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+        : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+        : "r"(remote));
     return v;
 }
 
@@ -237,13 +232,20 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
     for (int e = threadIdx.x; e < nvec; e += GATE_THREADS) {
         const int r = static_cast<int>(rank) * rows_per + (e * 4) / BN;
         const int c = (e * 4) % BN;
+        // all partial tiles' loads first, then the sum in rank order
+        float4 pv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (q < ks) pv[q] = ld_dsmem_f4(part + r * LDP + c, static_cast<uint32_t>(q));
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int q = 0; q < ks; ++q) {
-            const float4 v = ld_dsmem_f4(part + r * LDP + c, static_cast<uint32_t>(q));
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (q < ks) {
+                acc.x += pv[q].x;
+                acc.y += pv[q].y;
+                acc.z += pv[q].z;
+                acc.w += pv[q].w;
+            }
         }
         const int64_t gr = static_cast<int64_t>(mt) * GBM + r;
         if (gr < n) {

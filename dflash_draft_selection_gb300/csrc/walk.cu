@@ -11,8 +11,13 @@
 // One CTA per (request, position) gathers the 16 candidate rows of B and the
 // predecessor rows of A (16 candidates of the previous position, or the last
 // verified token at t = 0), scales A by the gate and computes the 16 x 16
-// score tile with fp32 FMAs from shared memory.  The CTA that finishes a
-// request's last tile (atomic ticket) walks the K tiles.
+// score tile with fp32 FMAs from shared memory, one thread per score.  It
+// also settles, for each of the 16 possible predecessors, the step's choice
+// and distribution.  The K CTAs of a request form a thread-block cluster:
+// after a cluster barrier the first CTA copies the K positions' tables out
+// of the others' shared memory and chains them from the last verified token.
+#include <cuda_bf16.h>
+
 #include "host.hpp"
 #include "common.cuh"
 
@@ -58,21 +63,63 @@ __device__ __forceinline__ void load_row_chunk(const void *table, int64_t row, i
     }
 }
 
-// The walk of request b by one warp over its K score tiles in shared memory.
-__device__ void walk_request(const WalkArgs &a, int64_t b, const float *sS, const int32_t *sC, int lane) {
+// Walk tables of one position's tile, for every predecessor row i: the row
+// is dead (it holds a NaN or only -inf), the chosen slot js (greedy: the
+// first maximum; sampled: the first slot whose cumulative q exceeds u, else
+// the last slot with q > 0) and the walk's distribution q over the row.
+// 256 threads: thread (i = tid / 16, j = tid % 16) holds S[i][j]; a row lives
+// in one half-warp.
+__device__ __forceinline__ void tile_tables(float v, bool greedy, float u, float *sQ, int32_t *sJs, int32_t *sDead,
+                                            int tid) {
+    const int i = tid >> 4, j = tid & 15;
+    const unsigned hw = 0xffffu << (tid & 16);  // this half-warp
+    float mx = v;
+#pragma unroll
+    for (int d = 8; d >= 1; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, d));  // NaN-ignoring
+    const bool any_nan = __ballot_sync(FULL, v != v) & hw;
+    const bool dead = any_nan || mx == NEG_INF;
+    int js = 0;
+    float q;
+    if (greedy) {
+        const uint32_t at = (__ballot_sync(FULL, v == mx) & hw) >> (tid & 16);
+        js = at ? __ffs(at) - 1 : 0;
+        q = j == js ? 1.0f : 0.0f;
+    } else {
+        const float e = dead ? 0.0f : expf(v - mx);
+        float tot = e;
+#pragma unroll
+        for (int d = 8; d >= 1; d >>= 1) tot += __shfl_xor_sync(FULL, tot, d);
+        float cum = e;
+#pragma unroll
+        for (int d = 1; d < 16; d <<= 1) {
+            const float t = __shfl_up_sync(FULL, cum, d);
+            if (j >= d) cum += t;
+        }
+        const float thr = u * tot;
+        const uint32_t hit = (__ballot_sync(FULL, cum > thr) & hw) >> (tid & 16);
+        const uint32_t pos = (__ballot_sync(FULL, e > 0.0f) & hw) >> (tid & 16);
+        js = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+        q = e / tot;
+    }
+    sQ[i * NC + j] = dead ? NAN : q;
+    if (j == 0) {
+        sJs[i] = js;
+        sDead[i] = dead ? 1 : 0;
+    }
+}
+
+// The walk of request b (one warp) over the K positions' tables: from the
+// last verified token (row 0 of position 0), each step takes the chosen slot
+// of the predecessor's row; a dead row ends the walk (that step and the rest
+// get token -1, slot -1 and NaN q).
+__device__ void walk_request(const WalkArgs &a, int64_t b, const float *sQ, const int32_t *sJs,
+                             const int32_t *sDead, const int32_t *sC, int lane) {
     const int K = a.K;
-    const float T = a.params ? a.params[b].temperature : 0.0f;
-    const bool greedy = !(T > 0.0f);
     int prev = 0;
     bool dead = false;
     for (int t = 0; t < K; ++t) {
-        const float v = lane < NC ? sS[(t * NC + prev) * NC + lane] : NEG_INF;
         const int64_t o = b * K + t;
-        const bool isn = lane < NC && v != v;
-        float mx = v;
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, d));
-        dead = dead || __any_sync(FULL, isn) || mx == NEG_INF;
+        dead = dead || sDead[t * NC + prev] != 0;
         if (dead) {
             if (lane < NC) a.q_sel[o * NC + lane] = NAN;
             if (lane == 0) {
@@ -81,32 +128,8 @@ __device__ void walk_request(const WalkArgs &a, int64_t b, const float *sS, cons
             }
             continue;
         }
-        int js;
-        float q;
-        if (greedy) {
-            const uint32_t at = __ballot_sync(FULL, lane < NC && v == mx);
-            js = __ffs(at) - 1;
-            q = lane == js ? 1.0f : 0.0f;
-        } else {
-            const float e = lane < NC ? expf(v - mx) : 0.0f;
-            const float tot = warp_sum(e);
-            float cum = e;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float tt = __shfl_up_sync(FULL, cum, d);
-                if (lane >= d) cum += tt;
-            }
-            const float thr = a.u_walk[o] * tot;
-            const uint32_t hit = __ballot_sync(FULL, lane < NC && cum > thr);
-            if (hit) {
-                js = __ffs(hit) - 1;
-            } else {
-                const uint32_t pos = __ballot_sync(FULL, lane < NC && e > 0.0f);
-                js = 31 - __clz(pos);
-            }
-            q = e / tot;
-        }
-        if (lane < NC) a.q_sel[o * NC + lane] = q;
+        const int js = sJs[t * NC + prev];
+        if (lane < NC) a.q_sel[o * NC + lane] = sQ[(t * NC + prev) * NC + lane];
         if (lane == 0) {
             a.path_slot[o] = js;
             a.path_tok[o] = sC[t * NC + js];
@@ -115,24 +138,59 @@ __device__ void walk_request(const WalkArgs &a, int64_t b, const float *sS, cons
     }
 }
 
+// Warp-level bf16 tensor-core product (m16n8k16, fp32 accumulation).
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// x as the sum of three bf16 (each the nearest bf16 of what remains): the
+// parts carry about 24 significant bits, fp32's precision.
+__device__ __forceinline__ void split_bf16(float x, uint16_t &hi, uint16_t &mid, uint16_t &lo) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(x);
+    const float r1 = x - __bfloat162float(h);
+    const __nv_bfloat16 m = __float2bfloat16_rn(r1);
+    const __nv_bfloat16 l = __float2bfloat16_rn(r1 - __bfloat162float(m));
+    hi = __bfloat16_as_ushort(h);
+    mid = __bfloat16_as_ushort(m);
+    lo = __bfloat16_as_ushort(l);
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(WALK_THREADS) k_pair_score_walk(WalkArgs a) {
+__global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a) {
     extern __shared__ float4 smem4[];
-    float *smem = reinterpret_cast<float *>(smem4);
+    unsigned char *base = reinterpret_cast<unsigned char *>(smem4);
     const int D = a.D;
-    const int LD = D + 4;  // padded row stride (floats)
-    float *sA = smem;               // [16][LD]  A(pred) * gate
-    float *sB = sA + NC * LD;       // [16][LD]  B(cand)
-    float *sG = sB + NC * LD;       // [D]
-    float *sU = sG + D;             // [16]
+    const int K = a.K;
+    // Operand rows.  bf16 tables: A(pred) * gate split into three bf16 parts
+    // and B(cand) as stored, rows of D + 8 bf16 (the pad spreads the rows
+    // over the banks); f32 tables: fp32 rows of D + 4.
+    const int LDH = D + 8, LDF = D + 4;
+    const size_t opbytes = BF16 ? 4 * NC * LDH * sizeof(uint16_t) : 2 * NC * LDF * sizeof(float);
+    uint16_t *sAh = reinterpret_cast<uint16_t *>(base);
+    uint16_t *sAm = sAh + NC * LDH;
+    uint16_t *sAl = sAm + NC * LDH;
+    uint16_t *sBh = sAl + NC * LDH;
+    float *sAf = reinterpret_cast<float *>(base);
+    float *sBf = sAf + NC * LDF;
+    float *sG = reinterpret_cast<float *>(base + opbytes);  // [D]
+    float *sU = sG + D;                                      // [16]
     int32_t *sCand = reinterpret_cast<int32_t *>(sU + NC);  // [16]
     int32_t *sPred = sCand + NC;                              // [16]
-    float *sTile = reinterpret_cast<float *>(sPred + NC);    // [16][16]
-    __shared__ int s_last;
+    float *sQ = reinterpret_cast<float *>(sPred + NC);       // [16][16] this position's q rows
+    int32_t *sJs = reinterpret_cast<int32_t *>(sQ + NC * NC);  // [16]
+    int32_t *sDead = sJs + NC;                                  // [16]
+    float *sPart = reinterpret_cast<float *>(sDead + NC);      // [8][16][16] per-warp partial tiles
+    float *sQAll = sPart + 8 * NC * NC;                         // [K][16][16] (first CTA)
+    int32_t *sJsAll = reinterpret_cast<int32_t *>(sQAll + K * NC * NC);  // [K][16]
+    int32_t *sDeadAll = sJsAll + K * NC;                                   // [K][16]
+    int32_t *sCAll = sDeadAll + K * NC;                                    // [K][16]
 
-    const int t = blockIdx.x;
+    const int t = blockIdx.x;  // = rank in the request's cluster
     const int64_t b = blockIdx.y;
-    const int K = a.K;
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -149,113 +207,197 @@ __global__ void __launch_bounds__(WALK_THREADS) k_pair_score_walk(WalkArgs a) {
         sPred[tid] = p;
     }
     for (int k = tid; k < D; k += WALK_THREADS) sG[k] = a.gate[pos * D + k];
+    if (t == 0)
+        for (int i = tid; i < K * NC; i += WALK_THREADS) sCAll[i] = a.cand_idx[b * K * NC + i];
+    const float T = a.params ? a.params[b].temperature : 0.0f;
+    const bool greedy = !(T > 0.0f);
+    const float u = greedy ? 0.0f : a.u_walk[pos];
     __syncthreads();
 
-    // Gather: rows 0..15 are A(pred_i) * gate, rows 16..31 are B(cand_j).
+    // Gather: rows 0..15 are A(pred_i) * gate, rows 16..31 are B(cand_j);
+    // each thread issues up to 8 row-chunk loads before using any.
     const int chunks = D / 4;
-    for (int rr = warp; rr < 2 * NC; rr += WALK_THREADS / 32) {
-        const bool isA = rr < NC;
-        const int i = isA ? rr : rr - NC;
-        const int32_t id = isA ? sPred[i] : sCand[i];
-        const bool ok = id >= 0 && id < a.V;
-        float *dst = (isA ? sA : sB) + i * LD;
-        for (int c = lane; c < chunks; c += 32) {
-            float v[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (ok) load_row_chunk<BF16>(isA ? a.A : a.Bt, id, D, c * 4, v);
-            if (isA) {
+    const int total = 2 * NC * chunks;
+    for (int j0 = 0; j0 < total; j0 += 8 * WALK_THREADS) {
+        float v[8][4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] *= sG[c * 4 + e];
+        for (int w = 0; w < 8; ++w) {
+            const int j = j0 + w * WALK_THREADS + tid;
+            const int rr = j / chunks, c = j - rr * chunks;
+            const bool isA = rr < NC;
+            const int32_t id = j < total ? (isA ? sPred[rr] : sCand[rr - NC]) : -1;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[w][e] = 0.0f;
+            if (id >= 0 && id < a.V) load_row_chunk<BF16>(isA ? a.A : a.Bt, id, D, c * 4, v[w]);
+        }
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const int j = j0 + w * WALK_THREADS + tid;
+            if (j < total) {
+                const int rr = j / chunks, c = j - rr * chunks;
+                const bool isA = rr < NC;
+                if (isA) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) v[w][e] *= sG[c * 4 + e];
+                }
+                if (BF16) {
+                    uint16_t h[4], m[4], l[4];
+                    if (isA) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) split_bf16(v[w][e], h[e], m[e], l[e]);
+                        *reinterpret_cast<uint2 *>(sAh + rr * LDH + c * 4) =
+                            make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16), h[2] | (static_cast<uint32_t>(h[3]) << 16));
+                        *reinterpret_cast<uint2 *>(sAm + rr * LDH + c * 4) =
+                            make_uint2(m[0] | (static_cast<uint32_t>(m[1]) << 16), m[2] | (static_cast<uint32_t>(m[3]) << 16));
+                        *reinterpret_cast<uint2 *>(sAl + rr * LDH + c * 4) =
+                            make_uint2(l[0] | (static_cast<uint32_t>(l[1]) << 16), l[2] | (static_cast<uint32_t>(l[3]) << 16));
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) h[e] = static_cast<uint16_t>(__float_as_uint(v[w][e]) >> 16);  // exact
+                        *reinterpret_cast<uint2 *>(sBh + (rr - NC) * LDH + c * 4) =
+                            make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16), h[2] | (static_cast<uint32_t>(h[3]) << 16));
+                    }
+                } else {
+                    float *dst = (isA ? sAf + rr * LDF : sBf + (rr - NC) * LDF) + c * 4;
+                    *reinterpret_cast<float4 *>(dst) = make_float4(v[w][0], v[w][1], v[w][2], v[w][3]);
+                }
             }
-            *reinterpret_cast<float4 *>(dst + c * 4) = make_float4(v[0], v[1], v[2], v[3]);
         }
     }
     __syncthreads();
 
-    // 16 blocks of 4x4 outputs x 16 k-slices.  warp w holds blocks 2w, 2w+1.
-    {
-        const int blk = warp * 2 + (lane >> 4);
-        const int ks = lane & 15;
-        const int i0 = (blk >> 2) * 4;
-        const int j0 = (blk & 3) * 4;
-        float acc[4][4];
+    // The 16 x 16 dot products.  bf16: warp w takes k-steps w, w + 8, ... of
+    // 16 and both 8-column halves, on the tensor cores (the three parts of
+    // A, smallest first); the eight partial tiles are summed in warp order.  f32: one thread
+    // per score with fp32 FMAs.
+    float dot;
+    if (BF16) {
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        const int gid = lane >> 2, tig = lane & 3;
+        for (int ks = warp; ks < D / 16; ks += 8) {
+            const int k0 = ks * 16 + tig * 2;
+            uint32_t ah[4], am[4], al[4];
+            am[0] = *reinterpret_cast<const uint32_t *>(sAm + gid * LDH + k0);
+            am[1] = *reinterpret_cast<const uint32_t *>(sAm + (gid + 8) * LDH + k0);
+            am[2] = *reinterpret_cast<const uint32_t *>(sAm + gid * LDH + k0 + 8);
+            am[3] = *reinterpret_cast<const uint32_t *>(sAm + (gid + 8) * LDH + k0 + 8);
+            ah[0] = *reinterpret_cast<const uint32_t *>(sAh + gid * LDH + k0);
+            ah[1] = *reinterpret_cast<const uint32_t *>(sAh + (gid + 8) * LDH + k0);
+            ah[2] = *reinterpret_cast<const uint32_t *>(sAh + gid * LDH + k0 + 8);
+            ah[3] = *reinterpret_cast<const uint32_t *>(sAh + (gid + 8) * LDH + k0 + 8);
+            al[0] = *reinterpret_cast<const uint32_t *>(sAl + gid * LDH + k0);
+            al[1] = *reinterpret_cast<const uint32_t *>(sAl + (gid + 8) * LDH + k0);
+            al[2] = *reinterpret_cast<const uint32_t *>(sAl + gid * LDH + k0 + 8);
+            al[3] = *reinterpret_cast<const uint32_t *>(sAl + (gid + 8) * LDH + k0 + 8);
 #pragma unroll
-        for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) acc[ii][jj] = 0.0f;
-        for (int c = ks; c < chunks; c += 16) {
-            float4 av[4], bv[4];
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii) av[ii] = *reinterpret_cast<const float4 *>(sA + (i0 + ii) * LD + c * 4);
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) bv[jj] = *reinterpret_cast<const float4 *>(sB + (j0 + jj) * LD + c * 4);
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    float s = acc[ii][jj];
-                    s = fmaf(av[ii].x, bv[jj].x, s);
-                    s = fmaf(av[ii].y, bv[jj].y, s);
-                    s = fmaf(av[ii].z, bv[jj].z, s);
-                    s = fmaf(av[ii].w, bv[jj].w, s);
-                    acc[ii][jj] = s;
-                }
-        }
-#pragma unroll
-        for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                float s = acc[ii][jj];
-                s += __shfl_xor_sync(FULL, s, 1);
-                s += __shfl_xor_sync(FULL, s, 2);
-                s += __shfl_xor_sync(FULL, s, 4);
-                s += __shfl_xor_sync(FULL, s, 8);
-                acc[ii][jj] = s;
+            for (int nb = 0; nb < 2; ++nb) {
+                const uint16_t *br = sBh + (nb * 8 + gid) * LDH + k0;
+                const uint32_t b0 = *reinterpret_cast<const uint32_t *>(br);
+                const uint32_t b1 = *reinterpret_cast<const uint32_t *>(br + 8);
+                mma_bf16_16816(acc[nb], al, b0, b1);  // smallest parts first
+                mma_bf16_16816(acc[nb], am, b0, b1);
+                mma_bf16_16816(acc[nb], ah, b0, b1);
             }
-        if (ks == 0) {
-#pragma unroll
-            for (int ii = 0; ii < 4; ++ii)
-#pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int i = i0 + ii, j = j0 + jj;
-                    const int32_t p = sPred[i], c = sCand[j];
-                    float s;
-                    if (p == -2)
-                        s = NEG_INF;
-                    else if (p < 0 || p >= a.V || c < 0 || c >= a.V)
-                        s = NAN;
-                    else
-                        s = sU[j] + acc[ii][jj];
-                    sTile[i * NC + j] = s;
-                }
         }
+        // fragment (row gid / gid + 8, columns nb*8 + tig*2 + {0,1}) -> partial tile
+        float *pw = sPart + warp * NC * NC;
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+            const int c = nb * 8 + tig * 2;
+            *reinterpret_cast<float2 *>(pw + gid * NC + c) = make_float2(acc[nb][0], acc[nb][1]);
+            *reinterpret_cast<float2 *>(pw + (gid + 8) * NC + c) = make_float2(acc[nb][2], acc[nb][3]);
+        }
+        __syncthreads();
+        dot = 0.0f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) dot += sPart[w * NC * NC + tid];
+    } else {
+        const int i = tid >> 4, j = tid & 15;
+        const float *ar = sAf + i * LDF;
+        const float *br = sBf + j * LDF;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int c = 0; c < chunks; ++c) {
+            const float4 x = *reinterpret_cast<const float4 *>(ar + c * 4);
+            const float4 y = *reinterpret_cast<const float4 *>(br + c * 4);
+            acc[0] = fmaf(x.x, y.x, acc[0]);
+            acc[1] = fmaf(x.y, y.y, acc[1]);
+            acc[2] = fmaf(x.z, y.z, acc[2]);
+            acc[3] = fmaf(x.w, y.w, acc[3]);
+        }
+        dot = (acc[0] + acc[1]) + (acc[2] + acc[3]);
     }
-    __syncthreads();
-    a.scores[pos * NC * NC + tid] = sTile[tid];
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-        const int old = atomicAdd(&a.tickets[b], 1);
-        s_last = old == K - 1;
-        if (s_last) a.tickets[b] = 0;
+    float s;
+    {
+        const int i = tid >> 4, j = tid & 15;
+        const int32_t p = sPred[i], c = sCand[j];
+        if (p == -2)
+            s = NEG_INF;
+        else if (p < 0 || p >= a.V || c < 0 || c >= a.V)
+            s = NAN;
+        else
+            s = sU[j] + dot;
     }
+    tile_tables(s, greedy, u, sQ, sJs, sDead, tid);
     __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    // Last tile of request b: load the K tiles and candidate ids, then walk.
-    float *sS = smem;                                            // [K][16][16]
-    int32_t *sC = reinterpret_cast<int32_t *>(smem + K * NC * NC);  // [K][16]
-    __syncthreads();
-    for (int i = tid; i < K * NC * NC; i += WALK_THREADS) sS[i] = __ldcg(a.scores + b * K * NC * NC + i);
-    for (int i = tid; i < K * NC; i += WALK_THREADS) sC[i] = a.cand_idx[b * K * NC + i];
-    __syncthreads();
-    if (warp == 0) walk_request(a, b, sS, sC, lane);
+    cluster_sync();  // every position's tables are in its CTA's shared memory
+    a.scores[pos * NC * NC + tid] = s;
+    if (t == 0) {
+        for (int i = tid; i < K * NC * NC; i += WALK_THREADS)
+            sQAll[i] = ld_dsmem_f32(sQ + (i & (NC * NC - 1)), static_cast<uint32_t>(i / (NC * NC)));
+        for (int i = tid; i < K * NC; i += WALK_THREADS) {
+            const uint32_t r = static_cast<uint32_t>(i / NC);
+            sJsAll[i] = __float_as_int(ld_dsmem_f32(reinterpret_cast<const float *>(sJs + (i & (NC - 1))), r));
+            sDeadAll[i] = __float_as_int(ld_dsmem_f32(reinterpret_cast<const float *>(sDead + (i & (NC - 1))), r));
+        }
+        __syncthreads();
+        if (warp == 0) walk_request(a, b, sQAll, sJsAll, sDeadAll, sCAll, lane);
+    }
+    // The other CTAs' shared memory stays until the first CTA has read it
+    // (no memory is published here: a relaxed arrival).
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
 static size_t walk_smem(int D, int K) {
-    const size_t tile = (2 * NC * (D + 4) + D + NC) * sizeof(float) + 2 * NC * sizeof(int32_t) +
-                        NC * NC * sizeof(float);
-    const size_t walk = static_cast<size_t>(K) * NC * NC * sizeof(float) + K * NC * sizeof(int32_t);
-    return tile > walk ? tile : walk;
+    const size_t ops = 4 * NC * (D + 8) * sizeof(uint16_t) > 2 * NC * (D + 4) * sizeof(float)
+                           ? 4 * NC * (D + 8) * sizeof(uint16_t)
+                           : 2 * NC * (D + 4) * sizeof(float);
+    return ops + (D + NC) * sizeof(float) + 2 * NC * sizeof(int32_t) +
+           (NC * NC * sizeof(float) + 2 * NC * sizeof(int32_t)) + 8 * NC * NC * sizeof(float) +
+           static_cast<size_t>(K) * (NC * NC * sizeof(float) + 3 * NC * sizeof(int32_t));
+}
+
+// Launch one cluster of K CTAs per request (K up to 15: clusters above the
+// portable 8 are allowed on this GPU once the kernel opts in).
+template <bool BF16>
+static dflash2_status launch_walk(const WalkArgs &a, cudaStream_t s) {
+    const void *fn = reinterpret_cast<const void *>(&k_pair_score_walk<BF16>);
+    static int opted[64] = {0};
+    static std::mutex mu;
+    {
+        const int dev = current_device();
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64 && !opted[dev]) {
+            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            opted[dev] = 1;
+        }
+    }
+    blocks_per_sm(fn, WALK_THREADS, walk_smem(1024, DFLASH2_MAX_K));  // raises the shared-memory limit once
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.K), static_cast<unsigned>(a.B), 1);
+    cfg.blockDim = dim3(WALK_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = walk_smem(a.D, a.K);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.K);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_pair_score_walk<BF16>, a) != cudaSuccess) return DFLASH2_ERR_CUDA;
+    return after_launch();
 }
 
 }  // namespace dfl
@@ -303,18 +445,8 @@ extern "C" dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const in
     a.q_sel = q_sel;
     a.scores = scores;
     a.tickets = static_cast<int32_t *>(ws);
-    const size_t smem = walk_smem(D, K);
-    const dim3 grid(static_cast<unsigned>(K), static_cast<unsigned>(B));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const size_t smem_max = walk_smem(1024, DFLASH2_MAX_K);
-    if (tdt == DFLASH2_BF16) {
-        blocks_per_sm(reinterpret_cast<const void *>(&k_pair_score_walk<true>), WALK_THREADS, smem_max);
-        k_pair_score_walk<true><<<grid, WALK_THREADS, smem, s>>>(a);
-    } else {
-        blocks_per_sm(reinterpret_cast<const void *>(&k_pair_score_walk<false>), WALK_THREADS, smem_max);
-        k_pair_score_walk<false><<<grid, WALK_THREADS, smem, s>>>(a);
-    }
-    return after_launch();
+    return tdt == DFLASH2_BF16 ? launch_walk<true>(a, s) : launch_walk<false>(a, s);
 }
 
 // ---------------------------------------------------------------------------
