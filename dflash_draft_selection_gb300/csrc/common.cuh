@@ -94,6 +94,13 @@ __device__ __forceinline__ int atomic_add_acq_rel(int *p, int v) {
     return old;
 }
 
+// Programmatic dependent launch.  pdl_wait: block until the grids this one
+// depends on in the stream have completed and their memory is visible (a
+// no-op when the grid was launched in the ordinary way).  pdl_trigger: let
+// the next grid in the stream be launched before this one completes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Thread-block clusters.  cluster_sync: all threads of all CTAs of the
 // cluster (release / acquire); the warp reconverges first.
 __device__ __forceinline__ void cluster_sync() {

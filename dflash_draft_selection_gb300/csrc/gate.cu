@@ -9,7 +9,7 @@
 // tensor-core GEMM.  gate[n, D] = sigmoid(h[n, hidden] . W_g[D, hidden]^T),
 // both operands K-major.  A CTA owns a 128 x BN output tile and a slice of the
 // hidden (K) dimension: TMA (cp.async.bulk.tensor, 128-byte swizzle) stages
-// 128x64 and BNx64 bf16 tiles through a 4-deep mbarrier ring, one thread
+// 128x64 and BNx64 bf16 tiles through a 3-deep mbarrier ring, one thread
 // issues tcgen05.mma (kind::f16, fp32 accumulation in tensor memory), and
 // tcgen05.commit releases each stage.  The ks CTAs of one tile form a thread-
 // block cluster along K: each reads its fp32 accumulator out of tensor memory
@@ -28,7 +28,7 @@ static __device__ unsigned int g_err_gate;
 
 constexpr int GBM = 128;       // tile rows = tensor-memory lanes
 constexpr int GBK = 64;        // hidden elements per stage: one 128-byte swizzle row
-constexpr int GSTAGES = 4;
+constexpr int GSTAGES = 3;  // small enough to share an SM with two row-scan CTAs
 constexpr int GATE_THREADS = 128;
 
 template <int BN>
@@ -268,6 +268,11 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
     tc_fence_after();
     __syncwarp();
     if (warp == 1) tmem_dealloc(tmem, TCOLS);
+    // The gate reads nothing the grid before it writes, so it may run beside
+    // that grid (programmatic launch); it completes only after that grid, so
+    // the grids after it see both results.
+    pdl_trigger();
+    pdl_wait();
 }
 
 // f32: one warp per output element.
@@ -338,13 +343,14 @@ static dflash2_status launch_gate_tc(const void *h, int64_t n, int64_t hidden, c
     cfg.blockDim = dim3(GATE_THREADS, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = static_cast<unsigned>(ks);
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, k_gate_tc<BN>, tm_h, tm_w, gate, n, D, kblocks, ks) != cudaSuccess)
         return DFLASH2_ERR_CUDA;
     return after_launch();

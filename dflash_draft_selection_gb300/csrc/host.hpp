@@ -55,6 +55,17 @@ inline int blocks_per_sm(const void *func, int threads, size_t smem) {
     return n;
 }
 
+// A launch attribute that lets this grid start while the previous grid in
+// the stream is still running, as soon as that grid allows it (programmatic
+// dependent launch); the grid itself waits (pdl_wait) before it reads what
+// the previous grids wrote.
+inline cudaLaunchAttribute pdl_attribute() {
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    return a;
+}
+
 inline dflash2_status after_launch() {
     return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }

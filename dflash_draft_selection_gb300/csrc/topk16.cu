@@ -68,7 +68,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
         (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
+    // This grid reads its logits only after the grids before it completed;
+    // from then on the next grid (the context gate reads nothing written
+    // here) may start on the SMs this grid frees.
     scan_init(sm);
+    pdl_wait();
+    pdl_trigger();
     const int64_t begin = range_begin(g, blockIdx.x), end = range_begin(g, blockIdx.x + 1);
     const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
     if (w < SCAN_WARPS) {
@@ -126,8 +131,16 @@ static dflash2_status launch_topk16(const ScanGeom &g, const ScanWs &sw, int32_t
     const size_t smem = scan_smem_bytes();
     const void *fn = reinterpret_cast<const void *>(&k_topk16<SAMPLED, BF16>);
     const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.total);
-    k_topk16<SAMPLED, BF16><<<static_cast<unsigned>(grid), SCAN_THREADS, smem, stream>>>(g, sw, cand_idx, cand_U,
-                                                                                       lse);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(SCAN_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_topk16<SAMPLED, BF16>, g, sw, cand_idx, cand_U, lse) != cudaSuccess)
+        return DFLASH2_ERR_CUDA;
     return after_launch();
 }
 

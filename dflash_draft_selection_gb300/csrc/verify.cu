@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_ve
     const int lane = threadIdx.x & 31;
     const int w = threadIdx.x >> 5;
     scan_init(sm);
+    pdl_wait();  // nothing is read before the grids before this one completed
     const int64_t begin = range_begin(g, blockIdx.x), end = range_begin(g, blockIdx.x + 1);
     const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
     if (w < SCAN_WARPS) {
@@ -371,7 +372,15 @@ static dflash2_status launch_verify(const ScanGeom &g, const ScanWs &sw, const V
     const size_t smem = scan_smem_bytes();
     const void *fn = reinterpret_cast<const void *>(&k_verify<SAMPLED, BF16>);
     const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.total);
-    k_verify<SAMPLED, BF16><<<static_cast<unsigned>(grid), SCAN_THREADS, smem, stream>>>(g, sw, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(SCAN_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_verify<SAMPLED, BF16>, g, sw, a) != cudaSuccess) return DFLASH2_ERR_CUDA;
     return after_launch();
 }
 

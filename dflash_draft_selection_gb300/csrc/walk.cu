@@ -195,6 +195,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t pos = b * K + t;
+    pdl_wait();  // the candidates and the gate come from the grids before this one
 
     if (tid < NC) {
         sCand[tid] = a.cand_idx[pos * NC + tid];
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
     __syncwarp();
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    pdl_trigger();
 }
 
 static size_t walk_smem(int D, int K) {
@@ -389,13 +391,14 @@ static dflash2_status launch_walk(const WalkArgs &a, cudaStream_t s) {
     cfg.blockDim = dim3(WALK_THREADS, 1, 1);
     cfg.dynamicSmemBytes = walk_smem(a.D, a.K);
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(a.K);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, k_pair_score_walk<BF16>, a) != cudaSuccess) return DFLASH2_ERR_CUDA;
     return after_launch();
 }
