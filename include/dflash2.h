@@ -148,7 +148,9 @@ dflash2_status dflash2_ctx_gate(const void *h, dflash2_dtype dt, int64_t n, int6
  * take the first slot whose cumulative q exceeds u_walk.  A step whose row
  * holds a NaN, or only -inf, ends the walk: that step and the rest get
  * token -1, slot -1 and NaN q.  Ids outside [0, V) give NaN scores.
- * ws: dflash2_pair_score_walk_workspace_bytes(B).
+ * ws: dflash2_pair_score_walk_workspace_bytes(B) bytes (one ticket per
+ *   request; the current kernel keeps its per-request state in the shared
+ *   memory of the request's thread-block cluster and leaves ws untouched).
  * Errors: INVALID_ARG for NULL/misaligned pointers, B < 0, K outside 1..15,
  * D not a power of two in 16..1024, V < 16, u_walk NULL with params set.
  */
@@ -180,9 +182,10 @@ dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand
  *   - The first call on a device looks up the array's device address (once,
  *     with that device current); make that first call before any stream
  *     capture.
- *   - All calls share the one array: two calls that may overlap on the GPU
- *     (different streams, or different host threads) race and give wrong
- *     paths.  Order them on one stream or synchronise between them.
+ *   - All calls share the one array.  The walk keeps each request's state in
+ *     the shared memory of the request's thread-block cluster and does not
+ *     read the tickets, so calls that overlap on the GPU only race on
+ *     clearing the array, which does not change any result.
  */
 #define DFLASH2_WALK_NOALLOC_MAX_B 16384
 dflash2_status dflash2_pair_score_walk_noalloc(int64_t B, int32_t K, const int32_t *cand_idx,
