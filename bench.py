@@ -296,6 +296,11 @@ def run_ours(args, rank, world, local):
                 "kernels_us": {k: round(v * 1e3, 2) for k, v in kern.items()},
                 "step_bytes_frac_of_peak": round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9 / peak, 4)}
 
+    # ---- the drafter-side conv (not part of the 4-call step): its own HBM roofline ----
+    aux = None
+    if not args.no_kernel_pass:
+        aux = {"conv2tap": time_conv(dev, peak)}
+
     # ---- end to end through the public API with host buffers ----
     e2e = None
     if not args.no_e2e:
@@ -317,10 +322,40 @@ def run_ours(args, rank, world, local):
                            "timing": ("CUDA-graph replay of the 4-call chain (programmatic dependent launches: "
                                       "ctx_gate runs in topk16's tail)") if graphs else "eager launches",
                            "parallelism": f"replicas x{world}"},
-                "gpu_launches": 4 * args.steps, "clocks": clk, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu}
+                "gpu_launches": 4 * args.steps, "clocks": clk, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
+                "aux": aux}
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def time_conv(dev, peak, reps=50):
+    """dflash2_conv2tap at the stress workload's conv shape ([256, 16, 5120] bf16, per-request x_prev):
+    mean of `reps` launches with CUDA events; every launch streams 170 MB (more than L2)."""
+    import torch
+
+    import dflash_draft_selection_gb300 as d2
+    from dflash_draft_selection_gb300 import synth
+    shp = synth.WORKLOADS["stress"]
+    g = torch.Generator(device=dev).manual_seed(shp.seed)
+    c = synth.make_conv(shp.B, shp.K + 1, shp.hidden, shp.dtype, g, dev)
+    y = torch.empty_like(c["x"])
+    for _ in range(3):
+        d2.conv2tap(c["x"], c["k0"], c["k1"], c["x_prev"], out=y)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        d2.conv2tap(c["x"], c["k0"], c["k1"], c["x_prev"], out=y)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    n = c["x"].numel()
+    algo = 4 * n * 2 + c["x_prev"].numel() * 2   # x, k0, k1 in; y out; x_prev
+    gbs = algo / (us * 1e-6) / 1e9
+    return {"workload": "stress conv [256, 16, 5120] bf16", "avg_launch_us": round(us, 2),
+            "algorithmic_bytes": algo, "achieved": round(gbs, 1), "unit": "GB/s", "peak": peak,
+            "frac": round(gbs / peak, 4), "bound": "hbm"}
 
 
 def run_e2e(chain, shp, dev, stream, steps, world):

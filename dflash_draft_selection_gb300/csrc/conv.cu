@@ -7,7 +7,7 @@
 // startup (conv_group_size divides the hidden size): with group size G, G
 // adjacent channels share one tap pair.
 //
-// A grid-stride elementwise stream.  bf16 outputs are the exact value of the
+// An elementwise stream.  bf16 outputs are the exact value of the
 // two products' sum rounded once to bf16: both products of bf16 operands are
 // exact in fp32, their fp32 sum s is corrected by the two-sum error e only
 // when s lies exactly on a bf16 rounding midpoint.
@@ -46,37 +46,41 @@ __device__ __forceinline__ float ldbf(const void *p, int64_t i) {
     return __uint_as_float(static_cast<uint32_t>(static_cast<const unsigned short *>(p)[i]) << 16);
 }
 
-// bf16, one tap pair per channel, H a multiple of 8: 16-byte vectors.
+// bf16, one tap pair per channel, H a multiple of 8: 16-byte vectors.  The
+// grid's y dimension walks the tokens (b, t) and x the token's channel
+// vectors, so a token's indices are computed once, not per vector.
 __global__ void __launch_bounds__(CONV_THREADS) k_conv_bf16_vec(ConvArgs a) {
-    const int64_t nvec = a.B * a.T * a.H / 8;
-    for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < nvec;
-         v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t e = v * 8;
-        const int64_t bt = e / a.H;
-        const int64_t c = e - bt * a.H;
+    const int64_t tokens = a.B * a.T;
+    const int64_t hv = a.H / 8;
+    for (int64_t bt = blockIdx.y; bt < tokens; bt += gridDim.y) {
         const int t = static_cast<int>(bt % a.T);
         const int64_t b = bt / a.T;
-        const uint4 xv = *reinterpret_cast<const uint4 *>(static_cast<const unsigned short *>(a.x) + e);
-        const uint4 pv = t == 0
-            ? *reinterpret_cast<const uint4 *>(static_cast<const unsigned short *>(a.x_prev) + b * a.H + c)
-            : *reinterpret_cast<const uint4 *>(static_cast<const unsigned short *>(a.x) + e - a.H);
-        const uint4 k0v = *reinterpret_cast<const uint4 *>(static_cast<const unsigned short *>(a.k0) + e);
-        const uint4 k1v = *reinterpret_cast<const uint4 *>(static_cast<const unsigned short *>(a.k1) + e);
-        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
-        const uint32_t ps[4] = {pv.x, pv.y, pv.z, pv.w};
-        const uint32_t k0s[4] = {k0v.x, k0v.y, k0v.z, k0v.w};
-        const uint32_t k1s[4] = {k1v.x, k1v.y, k1v.z, k1v.w};
-        uint32_t out[4];
+        const unsigned short *xr = static_cast<const unsigned short *>(a.x) + bt * a.H;
+        const unsigned short *pr = t == 0 ? static_cast<const unsigned short *>(a.x_prev) + b * a.H : xr - a.H;
+        const unsigned short *k0r = static_cast<const unsigned short *>(a.k0) + bt * a.H;
+        const unsigned short *k1r = static_cast<const unsigned short *>(a.k1) + bt * a.H;
+        unsigned short *yr = static_cast<unsigned short *>(a.y) + bt * a.H;
+        for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < hv;
+             v += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+            const uint4 xv = *reinterpret_cast<const uint4 *>(xr + v * 8);
+            const uint4 pv = *reinterpret_cast<const uint4 *>(pr + v * 8);
+            const uint4 k0v = *reinterpret_cast<const uint4 *>(k0r + v * 8);
+            const uint4 k1v = *reinterpret_cast<const uint4 *>(k1r + v * 8);
+            const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w};
+            const uint32_t ps[4] = {pv.x, pv.y, pv.z, pv.w};
+            const uint32_t k0s[4] = {k0v.x, k0v.y, k0v.z, k0v.w};
+            const uint32_t k1s[4] = {k1v.x, k1v.y, k1v.z, k1v.w};
+            uint32_t out[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const unsigned short lo =
-                round_pair_bf16(bf16lo(k0s[i]) * bf16lo(xs[i]), bf16lo(k1s[i]) * bf16lo(ps[i]));
-            const unsigned short hi =
-                round_pair_bf16(bf16hi(k0s[i]) * bf16hi(xs[i]), bf16hi(k1s[i]) * bf16hi(ps[i]));
-            out[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            for (int i = 0; i < 4; ++i) {
+                const unsigned short lo =
+                    round_pair_bf16(bf16lo(k0s[i]) * bf16lo(xs[i]), bf16lo(k1s[i]) * bf16lo(ps[i]));
+                const unsigned short hi =
+                    round_pair_bf16(bf16hi(k0s[i]) * bf16hi(xs[i]), bf16hi(k1s[i]) * bf16hi(ps[i]));
+                out[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+            }
+            *reinterpret_cast<uint4 *>(yr + v * 8) = make_uint4(out[0], out[1], out[2], out[3]);
         }
-        *reinterpret_cast<uint4 *>(static_cast<unsigned short *>(a.y) + e) =
-            make_uint4(out[0], out[1], out[2], out[3]);
     }
 }
 
@@ -127,9 +131,10 @@ extern "C" dflash2_status dflash2_conv2tap(const void *x, const void *k0, const 
     const bool vec = dt == DFLASH2_BF16 && group_size == 1 && H % 8 == 0 && aligned16(x) &&
                      aligned16(k0) && aligned16(k1) && aligned16(x_prev) && aligned16(y);
     if (vec) {
-        int64_t blocks = (n / 8 + CONV_THREADS - 1) / CONV_THREADS;
-        if (blocks > cap) blocks = cap;
-        k_conv_bf16_vec<<<static_cast<unsigned>(blocks), CONV_THREADS, 0, s>>>(a);
+        const int64_t tokens = B * T;
+        const int64_t xb = (H / 8 + CONV_THREADS - 1) / CONV_THREADS;
+        const int64_t yb = tokens < 65535 ? tokens : 65535;
+        k_conv_bf16_vec<<<dim3(static_cast<unsigned>(xb), static_cast<unsigned>(yb)), CONV_THREADS, 0, s>>>(a);
     } else {
         int64_t blocks = (n + CONV_THREADS - 1) / CONV_THREADS;
         if (blocks > cap) blocks = cap;

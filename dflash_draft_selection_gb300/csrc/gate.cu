@@ -11,8 +11,8 @@
 // hidden (K) dimension: TMA (cp.async.bulk.tensor, 128-byte swizzle) stages
 // 128x64 and BNx64 bf16 tiles through a 3-deep mbarrier ring, one thread
 // issues tcgen05.mma (kind::f16, fp32 accumulation in tensor memory), and
-// tcgen05.commit releases each stage.  The ks CTAs of one tile form a thread-
-// block cluster along K: each reads its fp32 accumulator out of tensor memory
+// tcgen05.commit releases each stage.  The ks CTAs (up to 8) of one tile
+// form a thread-block cluster along K: each reads its fp32 accumulator out of tensor memory
 // into shared memory, and after a cluster barrier each reduces 128/ks rows of
 // the tile across the cluster's shared memories (DSMEM, fixed order, so the
 // result does not depend on timing), applies the sigmoid and stores.
@@ -30,6 +30,7 @@ constexpr int GBM = 128;       // tile rows = tensor-memory lanes
 constexpr int GBK = 64;        // hidden elements per stage: one 128-byte swizzle row
 constexpr int GSTAGES = 3;  // small enough to share an SM with two row-scan CTAs
 constexpr int GATE_THREADS = 128;
+constexpr int MAX_KSPLIT = 8;  // CTAs of one tile's split-K cluster (16 measured slower)
 
 template <int BN>
 struct GateSmem {
@@ -233,13 +234,13 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
         const int r = static_cast<int>(rank) * rows_per + (e * 4) / BN;
         const int c = (e * 4) % BN;
         // all partial tiles' loads first, then the sum in rank order
-        float4 pv[8];
+        float4 pv[MAX_KSPLIT];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < MAX_KSPLIT; ++q)
             if (q < ks) pv[q] = ld_dsmem_f4(part + r * LDP + c, static_cast<uint32_t>(q));
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < MAX_KSPLIT; ++q) {
             if (q < ks) {
                 acc.x += pv[q].x;
                 acc.y += pv[q].y;
@@ -333,10 +334,23 @@ static dflash2_status launch_gate_tc(const void *h, int64_t n, int64_t hidden, c
     const int ntiles = D / BN;
     const int kblocks = static_cast<int>(hidden / GBK);
     const int64_t tiles = static_cast<int64_t>(mtiles) * ntiles;
+    // Split K until the CTAs fill two per SM (clusters of up to 16).
     int ks = 1;
-    while (ks < 8 && tiles * ks < sm_count() && ks * 2 <= kblocks) ks *= 2;
+    while (ks < MAX_KSPLIT && tiles * ks * 2 <= 2 * static_cast<int64_t>(sm_count()) && ks * 2 <= kblocks &&
+           GBM % (ks * 2) == 0)
+        ks *= 2;
     const size_t smem = sizeof(GateSmem<BN>) + 1024;
     const void *fn = reinterpret_cast<const void *>(&k_gate_tc<BN>);
+    {
+        static int opted[64] = {0};
+        static std::mutex mu;
+        const int dev = current_device();
+        std::lock_guard<std::mutex> lock(mu);
+        if (dev >= 0 && dev < 64 && !opted[dev]) {
+            cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            opted[dev] = 1;
+        }
+    }
     blocks_per_sm(fn, GATE_THREADS, smem);  // raises the shared-memory limit once per device
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(mtiles), static_cast<unsigned>(ntiles), static_cast<unsigned>(ks));

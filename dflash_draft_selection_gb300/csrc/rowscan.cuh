@@ -968,10 +968,12 @@ __device__ __forceinline__ int row_warps(const ScanGeom &g, int64_t row, int64_t
 }
 
 // Grid of a scan launch: as many CTAs as fit, at most MAX_SCAN_GRID and at
-// most one per chunk.
-inline int64_t scan_grid(int per_sm, int sms, int64_t total) {
+// most one per chunk.  When the rows alone nearly fill that many CTAs, one CTA
+// per row: no row is split, so no row waits for a join at the end.
+inline int64_t scan_grid(int per_sm, int sms, int64_t rows, int64_t total) {
     int64_t grid = static_cast<int64_t>(sms) * per_sm;
     if (grid > MAX_SCAN_GRID) grid = MAX_SCAN_GRID;
+    if (rows <= grid && rows * 8 >= grid * 7) return rows;
     if (grid > total) grid = total;
     return grid;
 }

@@ -130,7 +130,7 @@ static dflash2_status launch_topk16(const ScanGeom &g, const ScanWs &sw, int32_t
                                     float *lse, cudaStream_t stream) {
     const size_t smem = scan_smem_bytes();
     const void *fn = reinterpret_cast<const void *>(&k_topk16<SAMPLED, BF16>);
-    const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.total);
+    const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.rows, g.total);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(SCAN_THREADS, 1, 1);

@@ -371,7 +371,7 @@ static dflash2_status launch_verify(const ScanGeom &g, const ScanWs &sw, const V
                                     cudaStream_t stream) {
     const size_t smem = scan_smem_bytes();
     const void *fn = reinterpret_cast<const void *>(&k_verify<SAMPLED, BF16>);
-    const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.total);
+    const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.rows, g.total);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
     cfg.blockDim = dim3(SCAN_THREADS, 1, 1);
