@@ -84,6 +84,23 @@ __device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t 
         : "memory");
 }
 
+// An L2 cache policy for data read once: its lines are evicted first.
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// bulk_g2s with an L2 cache policy for the lines it reads.
+__device__ __forceinline__ void bulk_g2s_hint(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar,
+                                              uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_addr(sdst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+        : "memory");
+}
+
 // Atomic add at GPU scope with acquire and release semantics: the writes
 // that happen before it (this thread's, and those ordered before it by a
 // __syncwarp) are visible to whoever acquires the result, and it sees the

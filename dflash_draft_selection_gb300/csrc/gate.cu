@@ -167,6 +167,9 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    // The next grid may be scheduled once every CTA of this one is here; it
+    // waits for this grid to complete before it reads anything.
+    pdl_trigger();
 
     if (warp == 0 && lane == 0) {
         // TMA producer
@@ -272,7 +275,6 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
     // The gate reads nothing the grid before it writes, so it may run beside
     // that grid (programmatic launch); it completes only after that grid, so
     // the grids after it see both results.
-    pdl_trigger();
     pdl_wait();
 }
 

@@ -22,20 +22,24 @@
 // packed bf16x2 maxima and (for the log normaliser) its sum of 2^((x-m)c)
 // with packed f32x2 multiply-adds and adds.  Argmax: only lanes whose maximum
 // beats the warp's best value revisit their elements.  Best N elements: a
-// lane slice (the 8 KB chunk's 128 elements one lane holds) whose maximum
-// reaches the row's value floor is kept as one key (its maximum, its first
-// element); at least N elements reach the floor, which is the best of the
-// N-th largest lane maximum of the warps' first chunks (taken together
-// behind a named barrier), the warp's own N-th slice key and the best floor
-// the CTA's warps have published for the row.  The N best elements of a row
-// then lie in the slices whose maximum reaches the N-th largest slice maximum
-// F, and are ranked exactly from those slices alone at the end of the row.
+// lane slice (the chunk's 128 elements one lane holds) whose maximum reaches
+// the row's value floor is pushed as one key (its maximum, its first element)
+// to the warp's ring in shared memory.  While the row streams, the CTA's
+// completion warp drains the four rings into the row's sorted list of best
+// slice keys and publishes the value of its N-th key as the floor.  At least N
+// elements reach the floor, the best of that value and the N-th largest of the
+// maxima of disjoint halves of the lane slices of the warps' first chunks of
+// the row (taken together behind a named barrier).  The N best elements of
+// the row then lie in the slices whose maximum reaches the N-th largest slice
+// maximum F, and are ranked exactly from those slices alone, re-read once at
+// the end of the row.
 //
-// Row ends.  The streaming warps hand each row's partial results (sorted
-// slice lists, sums, argmax keys) to the CTA's completion warp through
-// double-buffered shared slots and stream on; the completion warp merges
-// them, joins the CTAs of a split row, ranks the row's elements and writes
-// the outputs, and clears the row's shared state before it frees the slot.
+// Row ends.  The streaming warps hand each row's partial results (sums,
+// argmax keys, their ring position) to the completion warp through
+// double-buffered shared slots and stream on; the completion warp finishes
+// the row's rings, joins the CTAs of a split row, ranks the row's elements
+// and writes the outputs, and clears the row's shared state before it frees
+// the slot.
 //
 // Waits are bounded: a warp that times out raises the error word, stops
 // issuing copies, waits a bounded time for those in flight and flags its rows.
@@ -52,7 +56,8 @@ constexpr int SCAN_THREADS = SCAN_WARPS * 32 + 32;  // + one completion warp
 constexpr int STREAM_THREADS = SCAN_WARPS * 32;
 constexpr int VEC_PER_CHUNK = CHUNK_BYTES / 16;
 constexpr int VEC_PER_LANE = VEC_PER_CHUNK / 32;
-constexpr int CAND_CAP = 64;          // candidate buffer of a warp (keys)
+constexpr int RING = 128;             // slice-key ring of a streaming warp (a power of two)
+constexpr int GCAP = 128;             // element keys the completion warp gathers at once (its scratch)
 constexpr int MAX_SCAN_GRID = 1024;   // CTAs of a scan launch (partial records are sized for it)
 constexpr long long WAIT_CYCLES = 4000000000ll;  // ~2 s at 2 GHz
 constexpr long long DRAIN_CYCLES = 200000000ll;  // ~0.1 s
@@ -124,16 +129,18 @@ struct ScanSmem {
     uint64_t full[SCAN_WARPS][WSTAGES];
     uint64_t slot_full[2], slot_empty[2];  // row hand-off (count SCAN_WARPS / 1)
     unsigned int floor_ord[2];             // CTA-wide value floor of a row (ordered bits), by row parity
-    uint32_t lmax[2][SCAN_WARPS][32];      // sorted lane maxima of each warp's first chunk of a row
-    uint64_t cand[SCAN_WARPS][CAND_CAP];     // slice-key buffers (empty between rows)
+    unsigned int ring_head[SCAN_WARPS];    // keys pushed to each warp's ring so far
+    unsigned int ring_tail[SCAN_WARPS];    // keys of each ring the completion warp has taken
+    uint32_t lmax[2][SCAN_WARPS][DFLASH2_MAX_TOPK];  // sorted half-slice maxima of each warp's first chunk of a row
+    uint64_t ring[SCAN_WARPS][RING];       // slice keys, position = count mod RING
     // Row results handed from the streaming warps to the completion warp.
     struct Hand {
-        uint64_t lists[SCAN_WARPS][DFLASH2_MAX_TOPK];
         uint64_t wbest[SCAN_WARPS];
         float wm[SCAN_WARPS], wsum[SCAN_WARPS];
         int bad[SCAN_WARPS];
+        unsigned int ring_end[SCAN_WARPS];  // 1 + the warp's ring count at its end of the row; 0 before
     } hand[2];
-    unsigned char scratch[1024];  // the completion warp's scratch (gathered keys, verify's draws)
+    alignas(16) unsigned char scratch[GCAP * 8];  // the completion warp's gathered keys; verify's draws
     alignas(128) unsigned char buf[SCAN_WARPS][WSTAGES][CHUNK_BYTES];
 };
 
@@ -162,6 +169,8 @@ struct WarpStream {
     int cons_r;           // row of the next consume, relative to the CTA's first row
     int cons_k;           // chunks consumed
     int n_w;              // chunks of this warp in the CTA's range
+    uint32_t head;        // keys pushed to the warp's ring
+    uint64_t pol;         // L2 policy of the stream: read once, evicted first
     bool aborted;
 };
 
@@ -178,7 +187,8 @@ __device__ __forceinline__ void stream_issue(ScanSmem &sm, const ScanGeom &g, Wa
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(bar, bytes);
         if (bytes)
-            bulk_g2s(sm.buf[w][stage], ws.iss_row + static_cast<int64_t>(ws.iss_c) * CHUNK_BYTES, bytes, bar);
+            bulk_g2s_hint(sm.buf[w][stage], ws.iss_row + static_cast<int64_t>(ws.iss_c) * CHUNK_BYTES, bytes, bar,
+                          ws.pol);
     }
     __syncwarp();
     ++ws.iss_k;
@@ -199,6 +209,8 @@ __device__ __forceinline__ void stream_start(ScanSmem &sm, const ScanGeom &g, Wa
     ws.iss_row = g.base + r0 * g.ld_bytes;
     ws.cons_r = static_cast<int>(r0 - begin / g.cpr);
     ws.iss_k = ws.cons_k = 0;
+    ws.head = 0;
+    ws.pol = l2_policy_evict_first();
     ws.aborted = false;
     for (int i = 0; i < WSTAGES && ws.iss_k < ws.n_w; ++i) stream_issue(sm, g, ws, w, lane);
 }
@@ -212,18 +224,13 @@ __device__ __forceinline__ void stream_drain(ScanSmem &sm, const WarpStream &ws,
 
 // ------------------------------------------------------------ scan state ----
 // A lane slice is what one lane reads of a chunk: vectors lane + 32 q
-// (q < 8) of 16 bytes, 64 bf16 or 32 f32 elements.  Its key orders slices by
-// their maximum, then by the index of their first element (lower first); the
-// ragged end of a row (fewer than 16 bytes) enters as single elements, below
-// every slice of the same value.  Bit 31 of the low word tells them apart.
-__device__ __forceinline__ uint64_t slice_key(float vmax, uint32_t base) {
-    vmax = (vmax == 0.0f) ? 0.0f : vmax;
-    return (static_cast<uint64_t>(f2ord(vmax)) << 32) | static_cast<uint32_t>(~base);
-}
-__device__ __forceinline__ uint64_t tail_key(float x, uint32_t idx) {
-    x = (x == 0.0f) ? 0.0f : x;
-    return (static_cast<uint64_t>(f2ord(x)) << 32) | (~idx & 0x7fffffffu);
-}
+// (q < 16) of 16 bytes, 128 bf16 or 64 f32 elements.  Its key orders slices
+// by their maximum, then by the index of their first element (lower first):
+// no element of the slice has a larger key.  The ragged end of a row (fewer
+// than 16 bytes) enters as single elements, whose key sits just below their
+// own element key; bit 31 of the low word tells them apart.
+__device__ __forceinline__ uint64_t slice_key(float vmax, uint32_t base) { return make_key(vmax, base); }
+__device__ __forceinline__ uint64_t tail_key(float x, uint32_t idx) { return make_key(x, idx) & ~0x80000000ull; }
 __device__ __forceinline__ bool key_is_slice(uint64_t k) { return (static_cast<uint32_t>(k) & 0x80000000u) != 0; }
 __device__ __forceinline__ uint32_t key_base(uint64_t k) { return ~static_cast<uint32_t>(k) & 0x7fffffffu; }
 
@@ -248,11 +255,8 @@ struct ScanState {
     float bw;   // argmax: the warp's best value (warp-uniform)
     float m, negmc, c;
     uint64_t acc[4];  // sum of 2^((x - m) c): eight partial sums as f32x2 pairs
-    float tau_val;    // value of the warp's N-th slice key (-inf while the list is short); warp-uniform
-    float lo;         // value floor: at least N elements of the row reach it; warp-uniform
-    int nbuf;         // keys in the warp's slice buffer
+    float lo;          // value floor: at least N elements of the row reach it; warp-uniform
     bool bad;
-    WarpList<R> list;  // best slice keys of the warp
 };
 
 // A chunk's 16-byte vectors as one lane holds them in registers: vector q is
@@ -278,8 +282,9 @@ struct VecLoad<true> {
         const uint32_t mm = bmax2_nan(bmax2_nan(w.x, w.y), bmax2_nan(w.z, w.w));
         return fmax_nan(bf16lo(mm), bf16hi(mm));
     }
-    // NaN-propagating maximum of the lane's vectors (packed bf16x2 maxima).
-    __device__ __forceinline__ static float lane_max(const uint4 (&v)[VEC_PER_LANE]) {
+    // NaN-propagating maxima of two disjoint halves of the lane's elements
+    // (the low and the high bf16 of every word; packed bf16x2 maxima).
+    __device__ __forceinline__ static void lane_max2(const uint4 (&v)[VEC_PER_LANE], float &m0, float &m1) {
         uint32_t a[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) a[j] = NEG_WORD;
@@ -293,7 +298,8 @@ struct VecLoad<true> {
         }
         const uint32_t mm = bmax2_nan(bmax2_nan(bmax2_nan(a[0], a[1]), bmax2_nan(a[2], a[3])),
                                       bmax2_nan(bmax2_nan(a[4], a[5]), bmax2_nan(a[6], a[7])));
-        return fmax_nan(bf16lo(mm), bf16hi(mm));
+        m0 = bf16lo(mm);
+        m1 = bf16hi(mm);
     }
     // acc[j] += (2^(lo_j c + negmc), 2^(hi_j c + negmc)) for the bf16 pair in
     // word j of the vector (packed f32x2 arithmetic; cc, nn hold c and negmc
@@ -327,11 +333,13 @@ struct VecLoad<false> {
         return fmax_nan(fmax_nan(__uint_as_float(w.x), __uint_as_float(w.y)),
                         fmax_nan(__uint_as_float(w.z), __uint_as_float(w.w)));
     }
-    __device__ __forceinline__ static float lane_max(const uint4 (&v)[VEC_PER_LANE]) {
+    // NaN-propagating maxima of two disjoint halves of the lane's vectors.
+    __device__ __forceinline__ static void lane_max2(const uint4 (&v)[VEC_PER_LANE], float &m0, float &m1) {
         float a[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
 #pragma unroll
         for (int q = 0; q < VEC_PER_LANE; ++q) a[q & 3] = fmax_nan(a[q & 3], vmax(v[q]));
-        return fmax_nan(fmax_nan(a[0], a[1]), fmax_nan(a[2], a[3]));
+        m0 = fmax_nan(a[0], a[1]);
+        m1 = fmax_nan(a[2], a[3]);
     }
     __device__ __forceinline__ static void accumulate(uint4 w, uint64_t cc, uint64_t nn, uint64_t (&acc)[4]) {
         const uint64_t t0 = fma2(pack2(w.x, w.y), cc, nn), t1 = fma2(pack2(w.z, w.w), cc, nn);
@@ -413,41 +421,47 @@ __device__ __forceinline__ void merge_buffer(WarpList<R> &list, const uint64_t *
     }
 }
 
-// Sort the slice buffer into the warp's list and raise the warp's floor to
-// the value of its N-th slice key.
-template <int R>
-__device__ __forceinline__ void flush_candidates(ScanSmem &sm, ScanState<R> &st, const uint64_t *cand, int nsel,
-                                                 int lane, int rp) {
-    __syncwarp();
-    merge_buffer<R>(st.list, cand, st.nbuf, lane);
-    st.nbuf = 0;
-    __syncwarp();
-    const uint64_t tw = st.list.at(nsel - 1);
-    if (tw != 0 && key_val(tw) > st.tau_val) {
-        st.tau_val = key_val(tw);
-        publish_floor(sm, rp, st.tau_val, lane);
+// Push the keys of the lanes with `lf` to warp w's ring, waiting (bounded)
+// for the completion warp to make room.  False after a time-out (or once the
+// warp's stream gave up).  Warp-uniform.
+__device__ __forceinline__ bool ring_push(ScanSmem &sm, WarpStream &ws, int w, int lane, bool lf, uint64_t key) {
+    const uint32_t bal = __ballot_sync(FULL, lf);
+    if (bal == 0) return true;
+    if (ws.aborted) return false;
+    const uint32_t n = __popc(bal);
+    int ok = 1;
+    if (lane == 0) {
+        const long long t0 = clock64();
+        while (ws.head + n - *reinterpret_cast<volatile unsigned int *>(&sm.ring_tail[w]) > RING) {
+            if (clock64() - t0 > WAIT_CYCLES) {
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
     }
+    if (!__shfl_sync(FULL, ok, 0)) return false;
+    if (lf) sm.ring[w][(ws.head + __popc(bal & ((1u << lane) - 1u))) & (RING - 1)] = key;
+    __syncwarp();
+    ws.head += n;
+    if (lane == 0) {
+        __threadfence_block();
+        *reinterpret_cast<volatile unsigned int *>(&sm.ring_head[w]) = ws.head;
+    }
+    return true;
 }
 
-// Append the keys of the lanes with `lf` to the warp's buffer (one per
-// lane), flushing it first when they do not fit.  Warp-uniform.
-template <int R>
-__device__ __forceinline__ void take_slices(ScanSmem &sm, ScanState<R> &st, bool lf, float cmax, uint64_t key,
-                                            int nsel, int lane, uint64_t *cand, int rp) {
-    uint32_t bal = __ballot_sync(FULL, lf);
-    if (st.nbuf + __popc(bal) > CAND_CAP) {
-        flush_candidates<R>(sm, st, cand, nsel, lane, rp);
-        lf = lf && cmax >= st.tau_val;  // against the raised floor
-        bal = __ballot_sync(FULL, lf);
-    }
-    if (lf) cand[st.nbuf + __popc(bal & ((1u << lane) - 1u))] = key;
-    st.nbuf += __popc(bal);
-    __syncwarp();
+// A ring push that timed out: the row is bad and the warp's stream gives up.
+__device__ __forceinline__ void push_failed(WarpStream &ws, bool &bad, int lane, unsigned int *err_word) {
+    bad = true;
+    if (!ws.aborted && lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
+    ws.aborted = true;
 }
 
 // One element of the ragged end of a row (lane 0 holds it); warp-uniform.
 template <int R, int MODE>
-__device__ __forceinline__ void scan_one(ScanState<R> &st, float x, uint32_t idx, bool valid, int lane) {
+__device__ __forceinline__ void scan_one(ScanSmem &sm, WarpStream &ws, ScanState<R> &st, float x, uint32_t idx,
+                                         bool valid, int w, int lane, unsigned int *err_word) {
     if (valid && x != x) st.bad = true;
     if (MODE == MODE_ARGMAX) {
         if (valid && x > st.bv) {
@@ -467,41 +481,67 @@ __device__ __forceinline__ void scan_one(ScanState<R> &st, float x, uint32_t idx
             st.acc[0] = pack2(__float_as_uint(__uint_as_float(lo32(st.acc[0])) + ex2(fmaf(x, st.c, st.negmc))),
                               hi32(st.acc[0]));
     }
-    const bool c = valid && x == x && x >= fmaxf(st.lo, st.tau_val);
-    const uint32_t msk = __ballot_sync(FULL, c);
-    if (msk) {
-        const int l = __ffs(msk) - 1;
-        st.list.insert(tail_key(__shfl_sync(FULL, x, l), __shfl_sync(FULL, idx, l)), lane);
-    }
+    const bool c = valid && x == x && x >= st.lo;
+    if (!ring_push(sm, ws, w, lane, c, tail_key(x, idx))) push_failed(ws, st.bad, lane, err_word);
 }
 
-// First chunk of each warp in the row (modes TOPN*, N <= 32): every warp of
-// the row publishes the sorted maxima of its lanes, waits for the others
-// (named barrier over the row's `expect` warps, w0 the first of them) and
-// merges their lists: at least N elements reach the N-th largest of those
-// maxima, a floor from 4 chunks instead of one.  A warp whose chunk did not
+// First chunk of each warp in the row (modes TOPN*, N <= R * 32): each lane
+// offers the maxima m0, m1 of two disjoint halves of its slice; at least N
+// elements reach the N-th largest of them.  When several warps hold chunks
+// of the row (`expect` of them, from w0 on cyclically), each publishes its
+// sorted maxima, waits for the others (named barrier) and merges their lists:
+// a floor from up to 4 chunks instead of one.  A warp whose chunk did not
 // arrive takes part with -inf maxima, so the barrier always completes.
-__device__ __forceinline__ void cta_first_floor(ScanSmem &sm, float &lo, float cmax, int nsel, int expect, int w0,
-                                                int rp, int w, int lane) {
-    uint32_t o = f2ord(cmax == cmax ? cmax : NEG_INF);
-    o = warp_sort_desc(o, lane);
-    sm.lmax[rp][w][lane] = o;
-    row_barrier(rp, expect * 32);
+template <int R>
+__device__ __forceinline__ void first_floor(ScanSmem &sm, float &lo, float m0, float m1, int nsel, int expect, int w0,
+                                            int rp, int w, int lane) {
+    const uint32_t o0 = warp_sort_desc(f2ord(m0 == m0 ? m0 : NEG_INF), lane);
+    const uint32_t o1 = warp_sort_desc(f2ord(m1 == m1 ? m1 : NEG_INF), lane);
+    if (R == 1) {  // 32-bit lists: the top 32 of the lane maxima
+        uint32_t o = warp_merge_desc_u32(o0, o1, lane);
+        if (expect > 1) {
+            sm.lmax[rp][w][lane] = o;
+            row_barrier(rp, expect * 32);
 #pragma unroll 1
-    for (int i = 0; i < expect; ++i) {
-        const int u = (w0 + i) % SCAN_WARPS;
-        if (u != w) o = warp_merge_desc_u32(o, sm.lmax[rp][u][lane], lane);
+            for (int i = 0; i < expect; ++i) {
+                const int u = (w0 + i) % SCAN_WARPS;
+                if (u != w) o = warp_merge_desc_u32(o, sm.lmax[rp][u][lane], lane);
+            }
+        }
+        lo = fmaxf(lo, ord2f(__shfl_sync(FULL, o, nsel - 1)));
+        publish_floor(sm, rp, lo, lane);
+        return;
     }
-    const float f = ord2f(__shfl_sync(FULL, o, nsel - 1));
-    lo = fmaxf(lo, f);
+    WarpList<R> L, o;
+    L.clear();
+    o.clear();
+    L.k[0] = static_cast<uint64_t>(o0) << 32;
+    o.k[0] = static_cast<uint64_t>(o1) << 32;
+    L.merge(o, lane);
+    if (expect > 1) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) sm.lmax[rp][w][r * 32 + lane] = static_cast<uint32_t>(L.k[r] >> 32);
+        row_barrier(rp, expect * 32);
+#pragma unroll 1
+        for (int i = 0; i < expect; ++i) {
+            const int u = (w0 + i) % SCAN_WARPS;
+            if (u != w) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) o.k[r] = static_cast<uint64_t>(sm.lmax[rp][u][r * 32 + lane]) << 32;
+                L.merge(o, lane);
+            }
+        }
+    }
+    lo = fmaxf(lo, ord2f(static_cast<uint32_t>(L.at(nsel - 1) >> 32)));
+    publish_floor(sm, rp, lo, lane);
 }
 
-// One chunk of a row held in registers (`v`, lane maximum `cmax`), first
-// element e0.  Warp-uniform.
+// One chunk of a row held in registers (`v`: nvt vectors of data, lane
+// maximum `cmax`), first element e0.  Warp-uniform.
 template <int R, int MODE, bool BF16>
-__device__ __forceinline__ void consume_chunk(ScanSmem &sm, ScanState<R> &st, const uint4 (&v)[VEC_PER_LANE],
-                                              bool has_data, float cmax, uint32_t e0, int nsel, int w, int lane,
-                                              int rp) {
+__device__ __forceinline__ void consume_chunk(ScanSmem &sm, WarpStream &ws, ScanState<R> &st,
+                                              const uint4 (&v)[VEC_PER_LANE], int nvt, float cmax, uint32_t e0,
+                                              int w, int lane, int rp, unsigned int *err_word) {
     using VL = VecLoad<BF16>;
     constexpr int VE = VL::VE;
     if (cmax != cmax) st.bad = true;
@@ -545,17 +585,17 @@ __device__ __forceinline__ void consume_chunk(ScanSmem &sm, ScanState<R> &st, co
     uint32_t so = lane == 0 ? *reinterpret_cast<volatile unsigned int *>(&sm.floor_ord[rp]) : 0u;
     so = __shfl_sync(FULL, so, 0);
     if (so != 0) st.lo = fmaxf(st.lo, ord2f(so));
-    const bool lf = has_data && cmax >= fmaxf(st.lo, st.tau_val);
-    if (__any_sync(FULL, lf))
-        take_slices<R>(sm, st, lf, cmax, slice_key(cmax, e0 + lane * VE), nsel, lane, sm.cand[w], rp);
+    const bool lf = lane < nvt && cmax >= st.lo;  // NaN never passes
+    if (!ring_push(sm, ws, w, lane, lf, slice_key(cmax, e0 + lane * VE))) push_failed(ws, st.bad, lane, err_word);
 }
 
-__device__ __forceinline__ bool row_streams(const RowTask &t) { return t.mode != MODE_SKIP; }
-
 // A streaming warp's results for the row into hand-off slot rp; the warp's
-// arrival on slot_full[rp] (count SCAN_WARPS) publishes them.
+// arrival on slot_full[rp] (count SCAN_WARPS) publishes them.  Its ring count
+// goes last: once the completion warp sees it, it knows where the warp's keys
+// of the row end.
 template <int R>
-__device__ __forceinline__ void hand_off_warp(ScanSmem &sm, int rp, int w, int lane, const ScanState<R> &st) {
+__device__ __forceinline__ void hand_off_warp(ScanSmem &sm, const WarpStream &ws, int rp, int w, int lane,
+                                              const ScanState<R> &st) {
     ScanSmem::Hand &h = sm.hand[rp];
     const uint64_t kb = warp_max_u64(st.bi >= 0 ? make_key(st.bv, static_cast<uint32_t>(st.bi)) : 0);
     float mm = st.m, s = sum_sums(st.acc);
@@ -566,15 +606,15 @@ __device__ __forceinline__ void hand_off_warp(ScanSmem &sm, int rp, int w, int l
         lse_combine(mm, s, m2, s2, st.c);
     }
     const bool bad = __any_sync(FULL, st.bad);
-    st.list.store(h.lists[w], lane);
     if (lane == 0) {
         h.wbest[w] = kb;
         h.wm[w] = mm;
         h.wsum[w] = s;
         h.bad[w] = bad ? 1 : 0;
+        __threadfence_block();
+        *reinterpret_cast<volatile unsigned int *>(&h.ring_end[w]) = ws.head + 1u;
+        mbar_arrive(&sm.slot_full[rp]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.slot_full[rp]);
 }
 
 // A streaming warp's part of the CTA's row `rrel` (global row `row`):
@@ -594,7 +634,7 @@ __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpSt
     const int nsel = task.nsel;
     const int rp = rrel & 1;
 
-    // Slot rp (buffers, lists, floor) is free once row rrel - 2 was taken.
+    // Slot rp (hand-off, floor) is free once row rrel - 2 was taken.
     bool slot_ok = true;
     if (rrel >= 2) slot_ok = __all_sync(FULL, mbar_wait(&sm.slot_empty[rp], ((rrel >> 1) - 1) & 1, WAIT_CYCLES));
     if (!slot_ok && lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
@@ -609,10 +649,7 @@ __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpSt
     st.negmc = 0.0f;
     st.c = LOG2E / task.T;
     st.bad = !slot_ok;
-    st.list.clear();
-    st.tau_val = NEG_INF;
     st.lo = NEG_INF;
-    st.nbuf = 0;
 
     bool first = true;
     while (ws.cons_k < ws.n_w && ws.cons_r == rrel) {
@@ -642,20 +679,21 @@ __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpSt
             ++ws.cons_k;
             if (ws.iss_k < ws.n_w) stream_issue(sm, g, ws, w, lane);
         }
-        float cmax = NEG_INF;
-        if (compute) cmax = VL::lane_max(v);
-        if (MODE != MODE_ARGMAX && first && !skip && nsel <= 32 && expect > 1)
-            cta_first_floor(sm, st.lo, cmax, nsel, expect, w0, rp, w, lane);
+        float m0 = NEG_INF, m1 = NEG_INF;
+        if (compute) VL::lane_max2(v, m0, m1);
+        const float cmax = fmax_nan(m0, m1);
+        if (MODE != MODE_ARGMAX && first && !skip)
+            first_floor<R>(sm, st.lo, m0, m1, nsel, expect, w0, rp, w, lane);
         if (compute) {
             const uint32_t e0 = static_cast<uint32_t>(c) * CE;
-            consume_chunk<R, MODE, BF16>(sm, st, v, lane < nvt, cmax, e0, nsel, w, lane, rp);
+            consume_chunk<R, MODE, BF16>(sm, ws, st, v, nvt, cmax, e0, w, lane, rp, err_word);
             // Ragged end of the row (fewer than 16 bytes), read by lane 0.
             if (c == g.cpr - 1) {
                 const char *rbase = g.base + row * g.ld_bytes;
                 const int64_t cnt = g.V - e0;
                 for (int64_t i = e0 + bulk / esz; i < e0 + cnt; ++i) {
                     const float xi = lane == 0 ? VL::scalar(rbase, i) : NEG_INF;
-                    scan_one<R, MODE>(st, xi, static_cast<uint32_t>(i), lane == 0, lane);
+                    scan_one<R, MODE>(sm, ws, st, xi, static_cast<uint32_t>(i), lane == 0, w, lane, err_word);
                 }
             }
         }
@@ -669,19 +707,17 @@ __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpSt
         }
     }
 
-    // ---- sort the slice buffer into the list; hand the warp's part of the
-    // row to the completion warp ----
-    if (MODE != MODE_ARGMAX && st.nbuf > 0) flush_candidates<R>(sm, st, sm.cand[w], nsel, lane, rp);
-    hand_off_warp(sm, rp, w, lane, st);
+    hand_off_warp(sm, ws, rp, w, lane, st);
 }
 
-// Offer every element of the slices chosen by this warp's lanes (`take`,
-// slice or tail key `k`) that reaches `F` to the element list `out`, one
-// element per lane at a time; `otau` is out's N-th key.  A slice is visited
-// in groups of vectors of 64 elements.  Warp-uniform.
+// Offer every element that reaches `F` of the lane slice starting at element
+// `base` (or, with !slice, the single element `base` of value `x1`) to the
+// element list `out`, for the lanes with `take`, one element per lane at a
+// time; `otau` is out's N-th key.  A slice is visited in groups of vectors of
+// 64 elements.  Warp-uniform.
 template <int R, bool BF16>
-__device__ __forceinline__ void offer_slices(const ScanGeom &g, const char *rowp, bool take, uint64_t k, float F,
-                                             int nsel, int lane, WarpList<R> &out, uint64_t &otau) {
+__device__ __forceinline__ void offer_slices(const ScanGeom &g, const char *rowp, bool take, uint32_t base, bool slice,
+                                             float x1, float F, int nsel, int lane, WarpList<R> &out, uint64_t &otau) {
     using VL = VecLoad<BF16>;
     constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
@@ -689,8 +725,6 @@ __device__ __forceinline__ void offer_slices(const ScanGeom &g, const char *rowp
     constexpr int GV = 64 / VE;                 // vectors per group
     constexpr int NG = VEC_PER_LANE / GV;       // groups per slice
     static_assert(NG * GV == VEC_PER_LANE, "slices split into whole groups");
-    const uint32_t base = key_base(k);
-    const bool slice = key_is_slice(k);
     int lin = 0, bulk = 0;
     if (slice) {
         const int c = static_cast<int>(base / CE);
@@ -728,7 +762,7 @@ __device__ __forceinline__ void offer_slices(const ScanGeom &g, const char *rowp
                     const uint32_t idx = base + (gi * GV + b / VE) * 32 * VE + (b % VE);
                     key = make_key(VL::scalar(rowp, idx), idx);
                 } else {
-                    key = make_key(key_val(k), base);
+                    key = make_key(x1, base);
                 }
                 if (key <= otau) key = 0;
             }
@@ -744,40 +778,121 @@ __device__ __forceinline__ void offer_slices(const ScanGeom &g, const char *rowp
     }
 }
 
-// Completion warp: the CTA's result for its row rrel (bounded wait for the
-// streaming warps' hand-offs; a time-out marks the row bad and stops further
-// waits), merged over the warps' sorted lists; then clear the row's shared
-// floor and free the slot.
-template <int R, int MODE>
-__device__ __forceinline__ void take_row(ScanSmem &sm, RowResult<R> &res, int rrel, float c, bool &aborted,
-                                         int lane, unsigned int *err_word) {
+// Completion warp: merge the batch's ring keys (one per lane, 0 for none)
+// whose value reaches the row's floor F into the row's list of best slice
+// keys (N-th key `tau`), then publish the list's N-th value as the floor.
+// Keys tied with F stay: the elements of tied slices are ranked by index.
+// Warp-uniform.
+template <int R>
+__device__ __forceinline__ void merge_ring_keys(ScanSmem &sm, uint64_t k, int rp, int nsel, WarpList<R> &list,
+                                                uint64_t &tau, int lane) {
+    uint32_t so = lane == 0 ? *reinterpret_cast<volatile unsigned int *>(&sm.floor_ord[rp]) : 0u;
+    so = __shfl_sync(FULL, so, 0);
+    float F = so != 0 ? ord2f(so) : NEG_INF;
+    if (tau != 0) F = fmaxf(F, key_val(tau));
+    const bool take = k != 0 && key_val(k) >= F;
+    if (!__any_sync(FULL, take)) return;
+    WarpList<R> o;
+    o.k[0] = warp_sort_desc(take ? k : 0ull, lane);
+#pragma unroll
+    for (int r = 1; r < R; ++r) o.k[r] = 0;
+    list.merge(o, lane);
+    const uint64_t t = list.at(nsel - 1);
+    if (t > tau) {
+        tau = t;
+        publish_floor(sm, rp, key_val(t), lane);
+    }
+}
+
+// Completion warp (modes TOPN*): the best slice keys of the CTA's part of
+// the row in slot rp.  Drains the four rings (taken positions `tail`, kept
+// across rows) while the streaming warps push to them, 32 keys a batch, until
+// every warp has handed the row off and its keys of the row are taken.  False
+// after a time-out with nothing to take.
+template <int R>
+__device__ __forceinline__ bool refine_row(ScanSmem &sm, int rp, int nsel, uint32_t (&tail)[SCAN_WARPS],
+                                           WarpList<R> &list, int lane) {
+    list.clear();
+    uint64_t tau = 0;
+    long long t0 = clock64();
+    while (true) {
+        uint64_t k = 0;
+        int nb = 0;
+        bool finished = true;
+#pragma unroll
+        for (int w = 0; w < SCAN_WARPS; ++w) {
+            // The ring count first, then the row-end mark: a warp that has
+            // left the row wrote its mark before pushing keys of the next.
+            uint32_t head = 0, re = 0;
+            if (lane == 0) {
+                head = *reinterpret_cast<volatile unsigned int *>(&sm.ring_head[w]);
+                __threadfence_block();
+                re = *reinterpret_cast<volatile unsigned int *>(&sm.hand[rp].ring_end[w]);
+            }
+            head = __shfl_sync(FULL, head, 0);
+            re = __shfl_sync(FULL, re, 0);
+            const uint32_t lim = re != 0 ? re - 1u : head;
+            const uint32_t avail = lim - tail[w];
+            const uint32_t room = static_cast<uint32_t>(32 - nb);
+            const uint32_t n = avail < room ? avail : room;
+            __syncwarp();
+            if (lane >= nb && lane < nb + static_cast<int>(n)) k = sm.ring[w][(tail[w] + (lane - nb)) & (RING - 1)];
+            tail[w] += n;
+            nb += static_cast<int>(n);
+            if (re == 0 || n < avail) finished = false;
+        }
+        if (nb > 0) {
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+#pragma unroll
+                for (int w = 0; w < SCAN_WARPS; ++w)
+                    *reinterpret_cast<volatile unsigned int *>(&sm.ring_tail[w]) = tail[w];
+            }
+            merge_ring_keys<R>(sm, k, rp, nsel, list, tau, lane);
+            t0 = clock64();
+        } else if (finished) {
+            return true;
+        } else {
+            if (clock64() - t0 > WAIT_CYCLES) return false;
+            __nanosleep(100);
+        }
+    }
+}
+
+// Completion warp: the CTA's result for its row rrel.  Modes TOPN* first
+// collect the row's best slice keys from the rings; then a bounded wait for the streaming
+// warps' hand-offs (a time-out marks the row bad and stops further waits),
+// merged over the warps; then clear the row's shared state and free the slot.
+template <int R, int MODE, bool BF16>
+__device__ __forceinline__ void take_row(ScanSmem &sm, const ScanGeom &g, int64_t row, RowResult<R> &res, int rrel,
+                                         float c, int nsel, uint32_t (&tail)[SCAN_WARPS], bool &aborted, int lane,
+                                         unsigned int *err_word) {
     const int rp = rrel & 1;
-    bool ok = !aborted && mbar_wait(&sm.slot_full[rp], (rrel >> 1) & 1, WAIT_CYCLES);
-    ok = __all_sync(FULL, ok);
-    if (!ok && !aborted && lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
-    if (!ok) aborted = true;
-    const ScanSmem::Hand &h = sm.hand[rp];
     res.list.clear();
     res.best = 0;
     res.m = NEG_INF;
     res.s = 0.0f;
+    bool ok = !aborted;
+    if (MODE != MODE_ARGMAX && ok) ok = refine_row<R>(sm, rp, nsel, tail, res.list, lane);
+    ok = ok && mbar_wait(&sm.slot_full[rp], (rrel >> 1) & 1, WAIT_CYCLES);
+    ok = __all_sync(FULL, ok);
+    if (!ok && !aborted && lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
+    if (!ok) aborted = true;
+    const ScanSmem::Hand &h = sm.hand[rp];
     res.bad = !ok;
     if (ok) {
         for (int u = 0; u < SCAN_WARPS; ++u) {
             res.bad |= h.bad[u] != 0;
-            if (MODE == MODE_ARGMAX) {
-                res.best = h.wbest[u] > res.best ? h.wbest[u] : res.best;
-            } else {
-                WarpList<R> o;
-                o.load(h.lists[u], lane);
-                res.list.merge(o, lane);
-                if (MODE == MODE_TOPN_LSE) lse_combine(res.m, res.s, h.wm[u], h.wsum[u], c);
-            }
+            if (MODE == MODE_ARGMAX) res.best = h.wbest[u] > res.best ? h.wbest[u] : res.best;
+            if (MODE == MODE_TOPN_LSE) lse_combine(res.m, res.s, h.wm[u], h.wsum[u], c);
         }
     }
     __syncwarp();
     if (lane == 0) {
         sm.floor_ord[rp] = 0;
+#pragma unroll
+        for (int u = 0; u < SCAN_WARPS; ++u) sm.hand[rp].ring_end[u] = 0;
         mbar_arrive(&sm.slot_empty[rp]);
     }
 }
@@ -785,11 +900,11 @@ __device__ __forceinline__ void take_row(ScanSmem &sm, RowResult<R> &res, int rr
 // Completion warp, once per row (modes TOPN*): the N best elements of the row
 // from its best slice keys L.  F, the N-th largest slice maximum, is reached
 // by at least N elements, so every one of the N best elements lies in a slice
-// whose maximum reaches F: re-read those slices, gather their elements that
-// reach F in shared memory and rank them.  If the list is full with its last
-// key tied at F (slices tied at F may have been left out), or the gathered
-// elements overflow the buffer, rank every slice of the row instead.
-// Returns element keys.
+// whose maximum reaches F: re-read those slices (all loads of a list register
+// in flight at once), gather their elements that reach F in shared memory and
+// rank them.  If the list is full with its last key tied at F (slices tied at
+// F may have been left out), or the gathered elements overflow the buffer,
+// rank every slice of the row instead.  Returns element keys.
 template <int R, bool BF16>
 __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t row, const WarpList<R> &L, int nsel,
                                                     unsigned char *scratch, int lane) {
@@ -797,7 +912,6 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
     constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
     constexpr int CE = CHUNK_BYTES / esz;
-    constexpr int GCAP = 1024 / 8;
     const char *rowp = g.base + row * g.ld_bytes;
     const uint64_t kN = L.at(nsel - 1);
     const float F = kN ? key_val(kN) : NEG_INF;
@@ -808,10 +922,9 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
     uint64_t *gbuf = reinterpret_cast<uint64_t *>(scratch);
     if (!(kL != 0 && key_val(kL) == F)) {
         // Lane p holds list entry p (p = r*32 + lane) and gathers the
-        // elements of its slice (or its single tail element) that reach F,
-        // half a slice (GV vectors) at a time: all loads of the half first,
-        // then a count, an offset from a warp scan, and the keys.
-        constexpr int GV = VEC_PER_LANE / 2;
+        // elements of its slice (or its single tail element) that reach F:
+        // all loads first, then a count, an offset from a warp scan, and the
+        // keys.
         int total = 0;
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -825,36 +938,36 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
                 lin = static_cast<int>((base % CE) / VE);
                 nvt = static_cast<int>(chunk_bulk_bytes(g, c)) >> 4;
             }
+            uint4 v[VEC_PER_LANE];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint4 v[GV];
+            for (int q = 0; q < VEC_PER_LANE; ++q) {
+                v[q] = make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+                if (take && slice && lin + q * 32 < nvt)
+                    v[q] = __ldcg(reinterpret_cast<const uint4 *>(rowp + static_cast<int64_t>(base + q * 32 * VE) * esz));
+            }
+            int cnt = (take && !slice) ? 1 : 0;
 #pragma unroll
-                for (int j = 0; j < GV; ++j) {
-                    const int q = h * GV + j;
-                    const bool in = take && slice && lin + q * 32 < nvt;
-                    v[j] = make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
-                    if (in) v[j] = __ldcg(reinterpret_cast<const uint4 *>(rowp + static_cast<int64_t>(base + q * 32 * VE) * esz));
-                }
-                int cnt = (h == 0 && take && !slice) ? 1 : 0;
-#pragma unroll
-                for (int j = 0; j < GV; ++j) {
+            for (int q = 0; q < VEC_PER_LANE; ++q) {
+                if (take && slice && lin + q * 32 < nvt) {
                     float x[VE];
-                    VL::unpack(v[j], x);
+                    VL::unpack(v[q], x);
 #pragma unroll
                     for (int e = 0; e < VE; ++e) cnt += x[e] >= F;  // NaN never passes
                 }
-                const int incl = warp_inclusive_scan_i(cnt, lane);
-                int pos = total + incl - cnt;
-                total += __shfl_sync(FULL, incl, 31);
-                if (cnt > 0 && total <= GCAP) {
-                    if (h == 0 && take && !slice) gbuf[pos++] = make_key(key_val(k), base);
+            }
+            const int incl = warp_inclusive_scan_i(cnt, lane);
+            int pos = total + incl - cnt;
+            total += __shfl_sync(FULL, incl, 31);
+            if (cnt > 0 && total <= GCAP) {
+                if (!slice) gbuf[pos++] = make_key(key_val(k), base);
 #pragma unroll
-                    for (int j = 0; j < GV; ++j) {
+                for (int q = 0; q < VEC_PER_LANE; ++q) {
+                    if (take && slice && lin + q * 32 < nvt) {
                         float x[VE];
-                        VL::unpack(v[j], x);
+                        VL::unpack(v[q], x);
 #pragma unroll
                         for (int e = 0; e < VE; ++e)
-                            if (x[e] >= F) gbuf[pos++] = make_key(x[e], base + (h * GV + j) * 32 * VE + e);
+                            if (x[e] >= F) gbuf[pos++] = make_key(x[e], base + q * 32 * VE + e);
                     }
                 }
             }
@@ -868,15 +981,14 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
     for (int c = 0; c < g.cpr; ++c) {
         const uint32_t base = static_cast<uint32_t>(c) * CE + lane * VE;
         const bool take = lane * 16 < static_cast<int>(chunk_bulk_bytes(g, c));
-        offer_slices<R, BF16>(g, rowp, take, slice_key(F, base), F, nsel, lane, out, otau);
+        offer_slices<R, BF16>(g, rowp, take, base, true, 0.0f, F, nsel, lane, out, otau);
     }
     // the ragged end
     const int64_t tail0 = static_cast<int64_t>(g.cpr - 1) * CE + chunk_bulk_bytes(g, g.cpr - 1) / esz;
     const int64_t i = tail0 + lane;
     const float x = i < g.V ? VL::scalar(rowp, i) : NEG_INF;
     const bool take = i < g.V && x >= F;
-    offer_slices<R, BF16>(g, rowp, take, tail_key(x, static_cast<uint32_t>(i < g.V ? i : 0)), F, nsel, lane, out,
-                          otau);
+    offer_slices<R, BF16>(g, rowp, take, static_cast<uint32_t>(i < g.V ? i : 0), false, x, F, nsel, lane, out, otau);
     return out;
 }
 
@@ -948,6 +1060,10 @@ __device__ __forceinline__ void scan_init(ScanSmem &sm) {
             mbar_init(&sm.slot_empty[s], 1);
         }
         sm.floor_ord[0] = sm.floor_ord[1] = 0;
+        for (int w = 0; w < SCAN_WARPS; ++w) {
+            sm.ring_head[w] = sm.ring_tail[w] = 0;
+            sm.hand[0].ring_end[w] = sm.hand[1].ring_end[w] = 0;
+        }
         fence_barrier_init();
     }
     __syncthreads();

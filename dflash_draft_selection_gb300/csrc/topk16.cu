@@ -56,7 +56,7 @@ __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const Ro
 // SAMPLED: some request may sample (params given): lists of 64 keys and every
 // row mode; otherwise every row is greedy (top-16 and the log normaliser).
 // Warps 0..SCAN_WARPS-1 stream the CTA's rows; the last warp completes each
-// row (joins the CTAs of a split row, ranks its elements, writes outputs)
+// row (merges the warps' lists, joins the CTAs of a split row, writes outputs)
 // while the others stream the next.
 template <bool SAMPLED, bool BF16>
 __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_topk16(ScanGeom g, ScanWs sw,
@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
         return;
     }
     bool aborted = false;
+    uint32_t tail[SCAN_WARPS] = {0, 0, 0, 0};  // ring keys taken, per streaming warp
     for (int64_t row = r_first; row <= r_last; ++row) {
         const int rrel = static_cast<int>(row - r_first);
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, false);
@@ -102,13 +103,13 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
         RowResult<R> res;
         bool done;
         if (!SAMPLED || task.mode == MODE_TOPN_LSE) {
-            take_row<R, MODE_TOPN_LSE>(sm, res, rrel, c, aborted, lane, &g_err_topk);
+            take_row<R, MODE_TOPN_LSE, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
             done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, c, lane);
         } else if (task.mode == MODE_TOPN) {
-            take_row<R, MODE_TOPN>(sm, res, rrel, c, aborted, lane, &g_err_topk);
+            take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
             done = join_parts<R, MODE_TOPN>(g, sw, row, res, c, lane);
         } else {
-            take_row<R, MODE_ARGMAX>(sm, res, rrel, c, aborted, lane, &g_err_topk);
+            take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
             if (blockIdx.x == range_owner(g, row * g.cpr)) {
                 if (lane < NC) {
                     cand_idx[row * NC + lane] = -1;

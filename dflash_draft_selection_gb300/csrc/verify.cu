@@ -314,6 +314,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_ve
     const int w = threadIdx.x >> 5;
     scan_init(sm);
     pdl_wait();  // nothing is read before the grids before this one completed
+    pdl_trigger();  // the next grid waits for this one to complete before it reads anything
     const int64_t begin = range_begin(g, blockIdx.x), end = range_begin(g, blockIdx.x + 1);
     const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
     if (w < SCAN_WARPS) {
@@ -335,6 +336,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_ve
         return;
     }
     bool aborted = false;
+    uint32_t tail[SCAN_WARPS] = {0, 0, 0, 0};  // ring keys taken, per streaming warp
     for (int64_t row = r_first; row <= r_last; ++row) {
         const int rrel = static_cast<int>(row - r_first);
         const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
@@ -342,14 +344,14 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_ve
         RowResult<R> res;
         bool done;
         if (!SAMPLED || task.mode == MODE_ARGMAX) {
-            take_row<R, MODE_ARGMAX>(sm, res, rrel, LOG2E, aborted, lane, &g_err_verify);
+            take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
             done = join_parts<R, MODE_ARGMAX>(g, sw, row, res, LOG2E, lane);
         } else if (task.mode == MODE_TOPN) {
-            take_row<R, MODE_TOPN>(sm, res, rrel, LOG2E, aborted, lane, &g_err_verify);
+            take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
             done = join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
             if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, lane);
         } else {
-            take_row<R, MODE_ARGMAX>(sm, res, rrel, LOG2E, aborted, lane, &g_err_verify);
+            take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
             if (blockIdx.x == range_owner(g, row * g.cpr)) {
                 if (lane == 0) {
                     rec->n = 0;

@@ -195,6 +195,9 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t pos = b * K + t;
+    // The next grid may be scheduled once every CTA of this one is here; it
+    // waits for this grid to complete before it reads anything.
+    pdl_trigger();
     pdl_wait();  // the candidates and the gate come from the grids before this one
 
     if (tid < NC) {
@@ -358,7 +361,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
     __syncwarp();
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-    pdl_trigger();
 }
 
 static size_t walk_smem(int D, int K) {

@@ -50,6 +50,28 @@ def test_ties_zero_signs_and_duplicates(ref, dtype):
     compare(run_both(ref, z), "ties")
 
 
+@pytest.mark.parametrize("sampled", [False, True])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_tie_blocks_and_ramps_mid_row(ref, dtype, sampled):
+    """Rows whose candidates pile up after the first chunk: a block of tied
+    maxima, many spread-out ties, a dense tie cluster in one chunk, ascending
+    and descending ramps.  Some overflow a warp's candidate buffer after the
+    floor has risen and are ranked by the rescan; the rest are ranked from
+    the streamed lists alone.  Either way the result must be exact."""
+    V = 50000
+    g = torch.Generator().manual_seed(7)
+    z = torch.randn(8, V, generator=g) * 2
+    z[0, 20000:20000 + 4096] = 9.0      # a whole chunk of tied maxima
+    z[1, ::997] = 8.0                   # ~50 ties spread over the row
+    z[2, 30000:30070] = 8.0             # 70 ties inside one chunk
+    z[3] = torch.linspace(-5.0, 5.0, V)  # ascending: every chunk beats the last
+    z[4] = torch.linspace(5.0, -5.0, V)  # descending: the first chunk holds the best
+    z[5, 40000:40040] = z[5].max() + 1.0  # 40 ties near the row's end
+    z = z.to(dtype)
+    params = params_np(8, 1.0, 64, 1.0) if sampled else None
+    compare(run_both(ref, z, params=params), f"tie blocks sampled={sampled}")
+
+
 def test_padded_rows_ld_greater_than_V(ref):
     V, ld = 5000, 5008
     z = torch.randn(6, ld).bfloat16()
