@@ -131,6 +131,7 @@ struct ScanSmem {
     unsigned int floor_ord[2];             // CTA-wide value floor of a row (ordered bits), by row parity
     unsigned int ring_head[SCAN_WARPS];    // keys pushed to each warp's ring so far
     unsigned int ring_tail[SCAN_WARPS];    // keys of each ring the completion warp has taken
+    int ngather;                           // keys the completion warp has gathered into its scratch
     uint32_t lmax[2][SCAN_WARPS][DFLASH2_MAX_TOPK];  // sorted half-slice maxima of each warp's first chunk of a row
     uint64_t ring[SCAN_WARPS][RING];       // slice keys, position = count mod RING
     // Row results handed from the streaming warps to the completion warp.
@@ -901,13 +902,13 @@ __device__ __forceinline__ void take_row(ScanSmem &sm, const ScanGeom &g, int64_
 // from its best slice keys L.  F, the N-th largest slice maximum, is reached
 // by at least N elements, so every one of the N best elements lies in a slice
 // whose maximum reaches F: re-read those slices (all loads of a list register
-// in flight at once), gather their elements that reach F in shared memory and
-// rank them.  If the list is full with its last key tied at F (slices tied at
+// in flight at once), gather their elements that reach F in shared memory
+// (cursor `ngather`) and rank them.  If the list is full with its last key tied at F (slices tied at
 // F may have been left out), or the gathered elements overflow the buffer,
 // rank every slice of the row instead.  Returns element keys.
 template <int R, bool BF16>
 __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t row, const WarpList<R> &L, int nsel,
-                                                    unsigned char *scratch, int lane) {
+                                                    unsigned char *scratch, int *ngather, int lane) {
     using VL = VecLoad<BF16>;
     constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
@@ -921,14 +922,20 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
     uint64_t otau = 0;
     uint64_t *gbuf = reinterpret_cast<uint64_t *>(scratch);
     if (!(kL != 0 && key_val(kL) == F)) {
-        // Lane p holds list entry p (p = r*32 + lane) and gathers the
-        // elements of its slice (or its single tail element) that reach F:
-        // all loads first, then a count, an offset from a warp scan, and the
-        // keys.
-        int total = 0;
-#pragma unroll
+        // Lane p holds list entry p (p = r*32 + lane): it loads its slice
+        // (all loads in flight at once), marks the vectors whose maximum
+        // reaches F and appends their elements that reach F (or its single
+        // tail element) to the scratch through a shared cursor; the sort
+        // below makes their order irrelevant.  The per-element work runs in
+        // a rolled loop: this code runs once per row, cold, and stays small.
+        if (lane == 0) *ngather = 0;
+        __syncwarp();
+#pragma unroll 1
         for (int r = 0; r < R; ++r) {
-            const uint64_t k = L.k[r];
+            uint64_t k = L.k[0];
+#pragma unroll
+            for (int rr = 1; rr < R; ++rr)
+                if (rr == r) k = L.k[rr];
             const bool take = k != 0 && key_val(k) >= F;
             const uint32_t base = key_base(k);
             const bool slice = key_is_slice(k);
@@ -945,34 +952,36 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
                 if (take && slice && lin + q * 32 < nvt)
                     v[q] = __ldcg(reinterpret_cast<const uint4 *>(rowp + static_cast<int64_t>(base + q * 32 * VE) * esz));
             }
-            int cnt = (take && !slice) ? 1 : 0;
+            uint32_t qm = 0;
 #pragma unroll
-            for (int q = 0; q < VEC_PER_LANE; ++q) {
-                if (take && slice && lin + q * 32 < nvt) {
-                    float x[VE];
-                    VL::unpack(v[q], x);
-#pragma unroll
-                    for (int e = 0; e < VE; ++e) cnt += x[e] >= F;  // NaN never passes
-                }
+            for (int q = 0; q < VEC_PER_LANE; ++q)
+                if (take && slice && lin + q * 32 < nvt && VL::vmax(v[q]) >= F) qm |= 1u << q;  // NaN never passes
+            if (take && !slice) {
+                const int pos = atomicAdd(ngather, 1);
+                if (pos < GCAP) gbuf[pos] = make_key(key_val(k), base);
             }
-            const int incl = warp_inclusive_scan_i(cnt, lane);
-            int pos = total + incl - cnt;
-            total += __shfl_sync(FULL, incl, 31);
-            if (cnt > 0 && total <= GCAP) {
-                if (!slice) gbuf[pos++] = make_key(key_val(k), base);
+#pragma unroll 1
+            while (qm) {
+                const int q = __ffs(qm) - 1;
+                qm &= qm - 1;
+                uint4 u = v[0];
 #pragma unroll
-                for (int q = 0; q < VEC_PER_LANE; ++q) {
-                    if (take && slice && lin + q * 32 < nvt) {
-                        float x[VE];
-                        VL::unpack(v[q], x);
+                for (int j = 1; j < VEC_PER_LANE; ++j)
+                    if (j == q) u = v[j];
+                float x[VE];
+                VL::unpack(u, x);
+                const uint32_t i0 = base + static_cast<uint32_t>(q * 32 * VE);
 #pragma unroll
-                        for (int e = 0; e < VE; ++e)
-                            if (x[e] >= F) gbuf[pos++] = make_key(x[e], base + q * 32 * VE + e);
+                for (int e = 0; e < VE; ++e) {
+                    if (x[e] >= F) {
+                        const int pos = atomicAdd(ngather, 1);
+                        if (pos < GCAP) gbuf[pos] = make_key(x[e], i0 + e);
                     }
                 }
             }
         }
         __syncwarp();
+        const int total = *reinterpret_cast<volatile int *>(ngather);
         if (total <= GCAP) {
             merge_buffer<R>(out, gbuf, total, lane);
             return out;

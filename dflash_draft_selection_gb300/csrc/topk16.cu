@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
             continue;
         }
         if (done) {
-            if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, lane);
+            if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
             finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
         }
     }

@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_ve
         } else if (task.mode == MODE_TOPN) {
             take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
             done = join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
-            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, lane);
+            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
         } else {
             take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
             if (blockIdx.x == range_owner(g, row * g.cpr)) {
