@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     ap.add_argument("--no-kernel-pass", action="store_true")
     ap.add_argument("--eager", action="store_true", help="time eager launches instead of graph replays")
+    ap.add_argument("--graph-steps", type=int, default=6,
+                    help="consecutive steps captured in one CUDA graph (a multiple of the 3 input sets)")
     return ap.parse_args()
 
 
@@ -226,20 +228,32 @@ def run_ours(args, rank, world, local):
         chain.step(i)
     torch.cuda.synchronize()
 
-    graphs = []
+    # One graph of S consecutive steps (step i reads input set i mod 3), so that programmatic
+    # dependent launches also link one step's verify to the next step's topk16; single-step
+    # graphs cover K mod S.
+    graphs, multi = [], None
+    nsets = len(chain.sets)
+    S = 1 if args.graph_steps <= 1 else max(nsets, args.graph_steps // nsets * nsets)
     if not args.eager:
         cap = torch.cuda.Stream(device=dev)
         with torch.cuda.stream(cap):
-            for i in range(len(chain.sets)):
+            for i in range(nsets):
                 chain.step(i)          # warm the capture stream
             cap.synchronize()
-            for i in range(len(chain.sets)):
+            for i in range(nsets):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=cap):
                     chain.step(i)
                 graphs.append(g)
+            if S > 1:
+                multi = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(multi, stream=cap):
+                    for i in range(S):
+                        chain.step(i)
         for g in graphs:
             g.replay()
+        if multi is not None:
+            multi.replay()
         torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps ----
@@ -250,10 +264,14 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
-    for i in range(args.steps):
-        if graphs:
-            graphs[i % len(graphs)].replay()
-        else:
+    if graphs:
+        full = args.steps // S if multi is not None else 0
+        for _ in range(full):
+            multi.replay()
+        for i in range(full * S, args.steps):
+            graphs[i % nsets].replay()
+    else:
+        for i in range(args.steps):
             chain.step(i)
     ev1.record(stream)
     torch.cuda.synchronize()
@@ -319,8 +337,9 @@ def run_ours(args, rank, world, local):
                            "D": shp.D, "sampling": "greedy" if shp.temperature == 0 else
                            f"T={shp.temperature},top_k={shp.top_k},top_p={shp.top_p}",
                            "l2": "inputs larger than L2 (292 MB of logits per step), 3 rotating input sets",
-                           "timing": ("CUDA-graph replay of the 4-call chain (programmatic dependent launches: "
-                                      "ctx_gate runs in topk16's tail)") if graphs else "eager launches",
+                           "timing": (f"CUDA graphs of {S} consecutive steps of the 4-call chain (programmatic "
+                                      "dependent launches: ctx_gate runs in topk16's tail, each kernel is "
+                                      "scheduled before its predecessor completes)") if graphs else "eager launches",
                            "parallelism": f"replicas x{world}"},
                 "gpu_launches": 4 * args.steps, "clocks": clk, "roofline": roof, "e2e": e2e, "cpu_baseline": cpu,
                 "aux": aux}

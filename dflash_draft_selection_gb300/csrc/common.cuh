@@ -135,6 +135,14 @@ __device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank)
     return v;
 }
 
+// Store a 32-bit word into CTA `rank`'s shared memory at the address of
+// `local` in this CTA (made visible to that CTA by the next cluster barrier).
+__device__ __forceinline__ void st_dsmem_u32(void *local, uint32_t v, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
+}
+
 // NaN-propagating maxima.
 __device__ __forceinline__ float fmax_nan(float a, float b) {
     float d;

@@ -11,11 +11,11 @@
 // One CTA per (request, position) gathers the 16 candidate rows of B and the
 // predecessor rows of A (16 candidates of the previous position, or the last
 // verified token at t = 0), scales A by the gate and computes the 16 x 16
-// score tile with fp32 FMAs from shared memory, one thread per score.  It
-// also settles, for each of the 16 possible predecessors, the step's choice
-// and distribution.  The K CTAs of a request form a thread-block cluster:
-// after a cluster barrier the first CTA copies the K positions' tables out
-// of the others' shared memory and chains them from the last verified token.
+// score tile on the tensor cores.  It also settles, for each of the 16
+// possible predecessors, the step's choice and distribution, and stores these
+// tables straight into the shared memory of the first CTA of the request's
+// thread-block cluster; after one cluster barrier that CTA chains them from
+// the last verified token.
 #include <cuda_bf16.h>
 
 #include "host.hpp"
@@ -68,8 +68,9 @@ __device__ __forceinline__ void load_row_chunk(const void *table, int64_t row, i
 // first maximum; sampled: the first slot whose cumulative q exceeds u, else
 // the last slot with q > 0) and the walk's distribution q over the row.
 // 256 threads: thread (i = tid / 16, j = tid % 16) holds S[i][j]; a row lives
-// in one half-warp.
-__device__ __forceinline__ void tile_tables(float v, bool greedy, float u, float *sQ, int32_t *sJs, int32_t *sDead,
+// in one half-warp.  The tables go to the arrays dQ [16][16], dJs [16] and
+// dDead [16] of the cluster's first CTA (addresses as in this CTA).
+__device__ __forceinline__ void tile_tables(float v, bool greedy, float u, float *dQ, int32_t *dJs, int32_t *dDead,
                                             int tid) {
     const int i = tid >> 4, j = tid & 15;
     const unsigned hw = 0xffffu << (tid & 16);  // this half-warp
@@ -101,10 +102,10 @@ __device__ __forceinline__ void tile_tables(float v, bool greedy, float u, float
         js = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
         q = e / tot;
     }
-    sQ[i * NC + j] = dead ? NAN : q;
+    st_dsmem_u32(dQ + i * NC + j, __float_as_uint(dead ? NAN : q), 0);
     if (j == 0) {
-        sJs[i] = js;
-        sDead[i] = dead ? 1 : 0;
+        st_dsmem_u32(dJs + i, static_cast<uint32_t>(js), 0);
+        st_dsmem_u32(dDead + i, dead ? 1u : 0u, 0);
     }
 }
 
@@ -180,10 +181,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
     float *sU = sG + D;                                      // [16]
     int32_t *sCand = reinterpret_cast<int32_t *>(sU + NC);  // [16]
     int32_t *sPred = sCand + NC;                              // [16]
-    float *sQ = reinterpret_cast<float *>(sPred + NC);       // [16][16] this position's q rows
-    int32_t *sJs = reinterpret_cast<int32_t *>(sQ + NC * NC);  // [16]
-    int32_t *sDead = sJs + NC;                                  // [16]
-    float *sPart = reinterpret_cast<float *>(sDead + NC);      // [8][16][16] per-warp partial tiles
+    float *sPart = reinterpret_cast<float *>(sPred + NC);     // [8][16][16] per-warp partial tiles
     float *sQAll = sPart + 8 * NC * NC;                         // [K][16][16] (first CTA)
     int32_t *sJsAll = reinterpret_cast<int32_t *>(sQAll + K * NC * NC);  // [K][16]
     int32_t *sDeadAll = sJsAll + K * NC;                                   // [K][16]
@@ -195,9 +193,6 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t pos = b * K + t;
-    // The next grid may be scheduled once every CTA of this one is here; it
-    // waits for this grid to complete before it reads anything.
-    pdl_trigger();
     pdl_wait();  // the candidates and the gate come from the grids before this one
 
     if (tid < NC) {
@@ -341,34 +336,24 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
         else
             s = sU[j] + dot;
     }
-    tile_tables(s, greedy, u, sQ, sJs, sDead, tid);
-    __syncthreads();
-    cluster_sync();  // every position's tables are in its CTA's shared memory
+    tile_tables(s, greedy, u, sQAll + t * NC * NC, sJsAll + t * NC, sDeadAll + t * NC, tid);
     a.scores[pos * NC * NC + tid] = s;
-    if (t == 0) {
-        for (int i = tid; i < K * NC * NC; i += WALK_THREADS)
-            sQAll[i] = ld_dsmem_f32(sQ + (i & (NC * NC - 1)), static_cast<uint32_t>(i / (NC * NC)));
-        for (int i = tid; i < K * NC; i += WALK_THREADS) {
-            const uint32_t r = static_cast<uint32_t>(i / NC);
-            sJsAll[i] = __float_as_int(ld_dsmem_f32(reinterpret_cast<const float *>(sJs + (i & (NC - 1))), r));
-            sDeadAll[i] = __float_as_int(ld_dsmem_f32(reinterpret_cast<const float *>(sDead + (i & (NC - 1))), r));
-        }
-        __syncthreads();
-        if (warp == 0) walk_request(a, b, sQAll, sJsAll, sDeadAll, sCAll, lane);
-    }
-    // The other CTAs' shared memory stays until the first CTA has read it
-    // (no memory is published here: a relaxed arrival).
-    __syncwarp();
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+    // Every position's tables are in the first CTA once all have arrived
+    // (release / acquire); nothing reads another CTA's memory after this.
+    cluster_sync();
+    // The next grid (it waits for this one to complete before it reads
+    // anything) is scheduled only now: its CTAs then find the SMs free all
+    // at once.  Scheduled while this grid still held the SMs, some of them
+    // could start only when others of its own CTAs finished.
+    pdl_trigger();
+    if (t == 0 && warp == 0) walk_request(a, b, sQAll, sJsAll, sDeadAll, sCAll, lane);
 }
 
 static size_t walk_smem(int D, int K) {
     const size_t ops = 4 * NC * (D + 8) * sizeof(uint16_t) > 2 * NC * (D + 4) * sizeof(float)
                            ? 4 * NC * (D + 8) * sizeof(uint16_t)
                            : 2 * NC * (D + 4) * sizeof(float);
-    return ops + (D + NC) * sizeof(float) + 2 * NC * sizeof(int32_t) +
-           (NC * NC * sizeof(float) + 2 * NC * sizeof(int32_t)) + 8 * NC * NC * sizeof(float) +
+    return ops + (D + NC) * sizeof(float) + 2 * NC * sizeof(int32_t) + 8 * NC * NC * sizeof(float) +
            static_cast<size_t>(K) * (NC * NC * sizeof(float) + 3 * NC * sizeof(int32_t));
 }
 
