@@ -669,11 +669,16 @@ __device__ __forceinline__ void scan_row(ScanSmem &sm, const ScanGeom &g, WarpSt
         // Copy the lane's vectors into registers, then refill the stage.
         uint4 v[VEC_PER_LANE];
         const unsigned char *tile = sm.buf[w][stage];
+        if (compute && nvt == VEC_PER_CHUNK) {  // every chunk but a row's last
 #pragma unroll
-        for (int q = 0; q < VEC_PER_LANE; ++q) {
-            const int vi = lane + q * 32;
-            v[q] = (compute && vi < nvt) ? *reinterpret_cast<const uint4 *>(tile + vi * 16)
-                                         : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+            for (int q = 0; q < VEC_PER_LANE; ++q) v[q] = *reinterpret_cast<const uint4 *>(tile + (lane + q * 32) * 16);
+        } else {
+#pragma unroll
+            for (int q = 0; q < VEC_PER_LANE; ++q) {
+                const int vi = lane + q * 32;
+                v[q] = (compute && vi < nvt) ? *reinterpret_cast<const uint4 *>(tile + vi * 16)
+                                             : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+            }
         }
         __syncwarp();
         if (ok) {
@@ -816,27 +821,26 @@ __device__ __forceinline__ bool refine_row(ScanSmem &sm, int rp, int nsel, uint3
     list.clear();
     uint64_t tau = 0;
     long long t0 = clock64();
+    unsigned int nap = 128;  // ns; doubles while the rings stay empty
     while (true) {
+        // Lane w < 4 reads ring w's count, then its row-end mark: a warp that
+        // has left the row wrote its mark before pushing keys of the next.
+        uint32_t hv = 0, rv = 0;
+        if (lane < SCAN_WARPS) hv = *reinterpret_cast<volatile unsigned int *>(&sm.ring_head[lane]);
+        __threadfence_block();
+        if (lane < SCAN_WARPS) rv = *reinterpret_cast<volatile unsigned int *>(&sm.hand[rp].ring_end[lane]);
+        __syncwarp();  // the keys below are read by other lanes than the counts
         uint64_t k = 0;
         int nb = 0;
         bool finished = true;
 #pragma unroll
         for (int w = 0; w < SCAN_WARPS; ++w) {
-            // The ring count first, then the row-end mark: a warp that has
-            // left the row wrote its mark before pushing keys of the next.
-            uint32_t head = 0, re = 0;
-            if (lane == 0) {
-                head = *reinterpret_cast<volatile unsigned int *>(&sm.ring_head[w]);
-                __threadfence_block();
-                re = *reinterpret_cast<volatile unsigned int *>(&sm.hand[rp].ring_end[w]);
-            }
-            head = __shfl_sync(FULL, head, 0);
-            re = __shfl_sync(FULL, re, 0);
+            const uint32_t head = __shfl_sync(FULL, hv, w);
+            const uint32_t re = __shfl_sync(FULL, rv, w);
             const uint32_t lim = re != 0 ? re - 1u : head;
             const uint32_t avail = lim - tail[w];
             const uint32_t room = static_cast<uint32_t>(32 - nb);
             const uint32_t n = avail < room ? avail : room;
-            __syncwarp();
             if (lane >= nb && lane < nb + static_cast<int>(n)) k = sm.ring[w][(tail[w] + (lane - nb)) & (RING - 1)];
             tail[w] += n;
             nb += static_cast<int>(n);
@@ -852,11 +856,13 @@ __device__ __forceinline__ bool refine_row(ScanSmem &sm, int rp, int nsel, uint3
             }
             merge_ring_keys<R>(sm, k, rp, nsel, list, tau, lane);
             t0 = clock64();
+            nap = 128;
         } else if (finished) {
             return true;
         } else {
             if (clock64() - t0 > WAIT_CYCLES) return false;
-            __nanosleep(100);
+            __nanosleep(nap);
+            if (nap < 1600) nap *= 2;
         }
     }
 }
