@@ -45,24 +45,6 @@ struct WalkArgs {
     int32_t *tickets;
 };
 
-template <bool BF16>
-__device__ __forceinline__ void load_row_chunk(const void *table, int64_t row, int D, int k, float (&v)[4]) {
-    if (BF16) {
-        const uint2 w = *reinterpret_cast<const uint2 *>(static_cast<const unsigned short *>(table) +
-                                                         row * D + k);
-        v[0] = bf16lo(w.x);
-        v[1] = bf16hi(w.x);
-        v[2] = bf16lo(w.y);
-        v[3] = bf16hi(w.y);
-    } else {
-        const float4 f = *reinterpret_cast<const float4 *>(static_cast<const float *>(table) + row * D + k);
-        v[0] = f.x;
-        v[1] = f.y;
-        v[2] = f.z;
-        v[3] = f.w;
-    }
-}
-
 // Walk tables of one position's tile, for every predecessor row i: the row
 // is dead (it holds a NaN or only -inf), the chosen slot js (greedy: the
 // first maximum; sampled: the first slot whose cumulative q exceeds u, else
@@ -213,52 +195,67 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
     const float u = greedy ? 0.0f : a.u_walk[pos];
     __syncthreads();
 
-    // Gather: rows 0..15 are A(pred_i) * gate, rows 16..31 are B(cand_j);
-    // each thread issues up to 8 row-chunk loads before using any.
-    const int chunks = D / 4;
-    const int total = 2 * NC * chunks;
-    for (int j0 = 0; j0 < total; j0 += 8 * WALK_THREADS) {
-        float v[8][4];
+    // Gather: rows 0..15 are A(pred_i) * gate, rows 16..31 are B(cand_j), in
+    // 16-byte chunks.  D is a power of two, so a row has cpr = 2^lcpr chunks
+    // and a pass of the 256 threads covers rpp = 256 / cpr rows: thread tid
+    // takes chunk tid mod cpr of rows tid / cpr + k rpp, with up to four loads
+    // in flight before it uses any.
+    {
+        constexpr int VEPL = BF16 ? 8 : 4;  // elements per chunk
+        const int lcpr = __ffs(D / VEPL) - 1;
+        const int c = tid & ((1 << lcpr) - 1);
+        const int rpp = WALK_THREADS >> lcpr;
+        const int r0 = tid >> lcpr;
+        const int npass = (2 * NC + rpp - 1) / rpp;
+        for (int p0 = 0; p0 < npass; p0 += 4) {
+            uint4 v[4];
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const int j = j0 + w * WALK_THREADS + tid;
-            const int rr = j / chunks, c = j - rr * chunks;
-            const bool isA = rr < NC;
-            const int32_t id = j < total ? (isA ? sPred[rr] : sCand[rr - NC]) : -1;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[w][e] = 0.0f;
-            if (id >= 0 && id < a.V) load_row_chunk<BF16>(isA ? a.A : a.Bt, id, D, c * 4, v[w]);
-        }
-#pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const int j = j0 + w * WALK_THREADS + tid;
-            if (j < total) {
-                const int rr = j / chunks, c = j - rr * chunks;
-                const bool isA = rr < NC;
-                if (isA) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) v[w][e] *= sG[c * 4 + e];
+            for (int k = 0; k < 4; ++k) {
+                const int rr = r0 + (p0 + k) * rpp;
+                v[k] = make_uint4(0u, 0u, 0u, 0u);
+                if (p0 + k < npass && rr < 2 * NC) {
+                    const bool isA = rr < NC;
+                    const int32_t id = isA ? sPred[rr] : sCand[rr - NC];
+                    if (id >= 0 && id < a.V) {
+                        const char *tab = static_cast<const char *>(isA ? a.A : a.Bt);
+                        v[k] = *reinterpret_cast<const uint4 *>(tab + (static_cast<int64_t>(id) * D + c * VEPL) *
+                                                                          (BF16 ? 2 : 4));
+                    }
                 }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int rr = r0 + (p0 + k) * rpp;
+                if (!(p0 + k < npass && rr < 2 * NC)) continue;
                 if (BF16) {
-                    uint16_t h[4], m[4], l[4];
-                    if (isA) {
+                    if (rr < NC) {
+                        const uint32_t wv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+                        uint32_t ph[4], pm[4], pl[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) split_bf16(v[w][e], h[e], m[e], l[e]);
-                        *reinterpret_cast<uint2 *>(sAh + rr * LDH + c * 4) =
-                            make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16), h[2] | (static_cast<uint32_t>(h[3]) << 16));
-                        *reinterpret_cast<uint2 *>(sAm + rr * LDH + c * 4) =
-                            make_uint2(m[0] | (static_cast<uint32_t>(m[1]) << 16), m[2] | (static_cast<uint32_t>(m[3]) << 16));
-                        *reinterpret_cast<uint2 *>(sAl + rr * LDH + c * 4) =
-                            make_uint2(l[0] | (static_cast<uint32_t>(l[1]) << 16), l[2] | (static_cast<uint32_t>(l[3]) << 16));
+                        for (int e2 = 0; e2 < 4; ++e2) {
+                            uint16_t h0, m0, l0, h1, m1, l1;
+                            split_bf16(bf16lo(wv[e2]) * sG[c * 8 + 2 * e2], h0, m0, l0);
+                            split_bf16(bf16hi(wv[e2]) * sG[c * 8 + 2 * e2 + 1], h1, m1, l1);
+                            ph[e2] = h0 | (static_cast<uint32_t>(h1) << 16);
+                            pm[e2] = m0 | (static_cast<uint32_t>(m1) << 16);
+                            pl[e2] = l0 | (static_cast<uint32_t>(l1) << 16);
+                        }
+                        *reinterpret_cast<uint4 *>(sAh + rr * LDH + c * 8) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                        *reinterpret_cast<uint4 *>(sAm + rr * LDH + c * 8) = make_uint4(pm[0], pm[1], pm[2], pm[3]);
+                        *reinterpret_cast<uint4 *>(sAl + rr * LDH + c * 8) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
                     } else {
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) h[e] = static_cast<uint16_t>(__float_as_uint(v[w][e]) >> 16);  // exact
-                        *reinterpret_cast<uint2 *>(sBh + (rr - NC) * LDH + c * 4) =
-                            make_uint2(h[0] | (static_cast<uint32_t>(h[1]) << 16), h[2] | (static_cast<uint32_t>(h[3]) << 16));
+                        *reinterpret_cast<uint4 *>(sBh + (rr - NC) * LDH + c * 8) = v[k];  // exact
                     }
                 } else {
-                    float *dst = (isA ? sAf + rr * LDF : sBf + (rr - NC) * LDF) + c * 4;
-                    *reinterpret_cast<float4 *>(dst) = make_float4(v[w][0], v[w][1], v[w][2], v[w][3]);
+                    float4 f = make_float4(__uint_as_float(v[k].x), __uint_as_float(v[k].y),
+                                           __uint_as_float(v[k].z), __uint_as_float(v[k].w));
+                    if (rr < NC) {
+                        f.x *= sG[c * 4];
+                        f.y *= sG[c * 4 + 1];
+                        f.z *= sG[c * 4 + 2];
+                        f.w *= sG[c * 4 + 3];
+                    }
+                    *reinterpret_cast<float4 *>((rr < NC ? sAf + rr * LDF : sBf + (rr - NC) * LDF) + c * 4) = f;
                 }
             }
         }
@@ -315,7 +312,7 @@ __global__ void __launch_bounds__(WALK_THREADS, 4) k_pair_score_walk(WalkArgs a)
         const float *ar = sAf + i * LDF;
         const float *br = sBf + j * LDF;
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int c = 0; c < chunks; ++c) {
+        for (int c = 0; c < D / 4; ++c) {
             const float4 x = *reinterpret_cast<const float4 *>(ar + c * 4);
             const float4 y = *reinterpret_cast<const float4 *>(br + c * 4);
             acc[0] = fmaf(x.x, y.x, acc[0]);
