@@ -55,6 +55,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// mbar_try_wait with a suspend-time hint of `ns` nanoseconds: the thread
+// sleeps until the phase completes or about that long has passed.
+__device__ __forceinline__ bool mbar_try_wait_ns(uint64_t *bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete, giving up after
 // `max_cycles` SM clock cycles (the per-SM cycle counter is monotonic).
 // Returns false on time-out.

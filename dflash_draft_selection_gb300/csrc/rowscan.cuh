@@ -813,15 +813,17 @@ __device__ __forceinline__ void merge_ring_keys(ScanSmem &sm, uint64_t k, int rp
 // Completion warp (modes TOPN*): the best slice keys of the CTA's part of
 // the row in slot rp.  Drains the four rings (taken positions `tail`, kept
 // across rows) while the streaming warps push to them, 32 keys a batch, until
-// every warp has handed the row off and its keys of the row are taken.  False
-// after a time-out with nothing to take.
+// every warp has handed the row off and its keys of the row are taken.  While
+// the rings are empty it sleeps on the slot's hand-off barrier (phase
+// `parity`), which wakes it as soon as the last warp hands off.  False after
+// a time-out with nothing to take.
 template <int R>
-__device__ __forceinline__ bool refine_row(ScanSmem &sm, int rp, int nsel, uint32_t (&tail)[SCAN_WARPS],
-                                           WarpList<R> &list, int lane) {
+__device__ __forceinline__ bool refine_row(ScanSmem &sm, int rp, uint32_t parity, int nsel,
+                                           uint32_t (&tail)[SCAN_WARPS], WarpList<R> &list, int lane) {
     list.clear();
     uint64_t tau = 0;
     long long t0 = clock64();
-    unsigned int nap = 128;  // ns; doubles while the rings stay empty
+    unsigned int nap = 128;  // ns; doubles while the rings stay empty (the hand-off wakes the warp)
     while (true) {
         // Lane w < 4 reads ring w's count, then its row-end mark: a warp that
         // has left the row wrote its mark before pushing keys of the next.
@@ -861,7 +863,7 @@ __device__ __forceinline__ bool refine_row(ScanSmem &sm, int rp, int nsel, uint3
             return true;
         } else {
             if (clock64() - t0 > WAIT_CYCLES) return false;
-            __nanosleep(nap);
+            mbar_try_wait_ns(&sm.slot_full[rp], parity, nap);
             if (nap < 1600) nap *= 2;
         }
     }
@@ -881,7 +883,7 @@ __device__ __forceinline__ void take_row(ScanSmem &sm, const ScanGeom &g, int64_
     res.m = NEG_INF;
     res.s = 0.0f;
     bool ok = !aborted;
-    if (MODE != MODE_ARGMAX && ok) ok = refine_row<R>(sm, rp, nsel, tail, res.list, lane);
+    if (MODE != MODE_ARGMAX && ok) ok = refine_row<R>(sm, rp, (rrel >> 1) & 1, nsel, tail, res.list, lane);
     ok = ok && mbar_wait(&sm.slot_full[rp], (rrel >> 1) & 1, WAIT_CYCLES);
     ok = __all_sync(FULL, ok);
     if (!ok && !aborted && lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
