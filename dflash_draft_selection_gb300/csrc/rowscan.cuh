@@ -1086,10 +1086,12 @@ __device__ __forceinline__ void scan_init(ScanSmem &sm) {
     __syncthreads();
 }
 
-// CTAs per SM of a scan kernel: three for all-greedy launches, two when
-// requests may sample (two-register-row lists and more row modes).
-template <bool SAMPLED>
-constexpr int scan_min_blocks() { return SAMPLED ? 2 : 3; }
+// CTAs per SM of a scan kernel: three (the streaming warps hold no lists;
+// only the completion warp holds the row's list of 32 or 64 keys).  Verify
+// with sampling requests keeps two: its completion work per row (filters,
+// draws) is the longer part there, and measured faster at two.
+template <bool SAMPLED, bool VERIFY = false>
+constexpr int scan_min_blocks() { return SAMPLED && VERIFY ? 2 : 3; }
 
 // The CTA's part of row `row`: how many of the warps hold a chunk of it
 // (returned) and the first of them (*w0); they follow cyclically.

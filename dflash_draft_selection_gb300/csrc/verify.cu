@@ -302,7 +302,7 @@ __device__ void row_done(const VerifyArgs &a, const dflash2_sampling *params, in
 // row, writes its record and runs the accept walk of a completed request)
 // while the others stream the next.
 template <bool SAMPLED, bool BF16>
-__global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_verify(ScanGeom g, ScanWs sw,
+__global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()) k_verify(ScanGeom g, ScanWs sw,
                                                                                   VerifyArgs a) {
     constexpr int R = SAMPLED ? 2 : 1;
     extern __shared__ unsigned char smem_raw[];
