@@ -76,18 +76,15 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
                      smem_addr(bar))
                  : "memory");
 }
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 16 columns of the warp's 32 TMEM lanes into registers; the caller waits
+// (tcgen05.wait::ld) before reading them.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t *r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
         "%13, %14, %15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
-          "=r"(r[15])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tma_load_2d(void *sdst, const CUtensorMap *tmap, int x, int y, uint64_t *bar) {
     asm volatile(
@@ -215,15 +212,17 @@ __global__ void __launch_bounds__(GATE_THREADS) k_gate_tc(const __grid_constant_
     tc_fence_after();
     float *part = reinterpret_cast<float *>(&sm.a[0][0]);
     const int row = warp * 32 + lane;
+    // All of the warp's column blocks are loaded before one wait.
+    uint32_t bits[BN];
 #pragma unroll
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-        float v[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, v);
+    for (int c0 = 0; c0 < BN; c0 += 16) tmem_ld16_nowait(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, bits + c0);
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int i = 0; i < 16; i += 4) {
-            float4 q = ok ? make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]) : make_float4(NAN, NAN, NAN, NAN);
-            *reinterpret_cast<float4 *>(part + row * LDP + c0 + i) = q;
-        }
+    for (int i = 0; i < BN; i += 4) {
+        float4 q = ok ? make_float4(__uint_as_float(bits[i]), __uint_as_float(bits[i + 1]), __uint_as_float(bits[i + 2]),
+                                    __uint_as_float(bits[i + 3]))
+                      : make_float4(NAN, NAN, NAN, NAN);
+        *reinterpret_cast<float4 *>(part + row * LDP + i) = q;
     }
     if (!ok && threadIdx.x == 0) atomicOr(&g_err_gate, ERR_WAIT_TIMEOUT);
     tc_fence_before();
