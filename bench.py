@@ -71,11 +71,18 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def _code_only(text):
+    """C++ source without comments, trailing blanks and empty lines (edits to comments keep the hash)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_sha(kernel):
     h = hashlib.sha256()
     for n in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "dflash_draft_selection_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "dflash_draft_selection_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

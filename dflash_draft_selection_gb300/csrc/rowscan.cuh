@@ -11,12 +11,15 @@
 // A row that straddles two or more ranges is reduced by each of its CTAs; each
 // writes a partial result to the workspace and the CTA that completes the row
 // (a per-row ticket) combines the parts in CTA order and finishes the row.
+// When the rows alone nearly fill the CTA slots, each CTA takes one whole row
+// instead and no row is split.
 //
 // Streaming.  Chunk j of a CTA's range belongs to streaming warp j mod 4.
 // Each streaming warp streams its chunks through a private 2-stage
 // shared-memory ring filled by 1-D bulk copies (cp.async.bulk) that complete
 // on per-stage mbarriers.  A warp copies an arrived chunk into registers and
-// refills the stage at once, so two of its chunks are always in flight.
+// refills the stage at once, so two of its chunks are always in flight.  The
+// copies read with an L2 evict-first policy: the logits are read once.
 //
 // Per chunk, each lane takes the maximum of its 128 (bf16) elements with
 // packed bf16x2 maxima and (for the log normaliser) its sum of 2^((x-m)c)
