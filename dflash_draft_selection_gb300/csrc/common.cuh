@@ -87,17 +87,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// 1-D bulk copy global -> shared (non-multicast), completing on `bar`.
-// Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *sdst, const void *gsrc, uint32_t bytes,
-                                         uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(sdst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
 // An L2 cache policy for data read once: its lines are evicted first.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t pol;
@@ -105,7 +94,9 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return pol;
 }
 
-// bulk_g2s with an L2 cache policy for the lines it reads.
+// 1-D bulk copy global -> shared (non-multicast), completing on `bar`, with
+// an L2 cache policy for the lines it reads.  Both addresses 16-byte
+// aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s_hint(void *sdst, const void *gsrc, uint32_t bytes, uint64_t *bar,
                                               uint64_t pol) {
     asm volatile(
@@ -139,16 +130,6 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Read a float of CTA `rank`'s shared memory at the address of `local` in
-// this CTA (the data is stable between two cluster barriers).
-__device__ __forceinline__ float ld_dsmem_f32(const float *local, uint32_t rank) {
-    uint32_t remote;
-    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
-    float v;
-    asm("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote));
-    return v;
-}
-
 // Store a 32-bit word into CTA `rank`'s shared memory at the address of
 // `local` in this CTA (made visible to that CTA by the next cluster barrier).
 __device__ __forceinline__ void st_dsmem_u32(void *local, uint32_t v, uint32_t rank) {

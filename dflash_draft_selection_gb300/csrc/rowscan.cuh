@@ -56,7 +56,6 @@ constexpr int CHUNK_BYTES = 8192;
 constexpr int WSTAGES = 2;
 constexpr int SCAN_WARPS = 4;
 constexpr int SCAN_THREADS = SCAN_WARPS * 32 + 32;  // + one completion warp
-constexpr int STREAM_THREADS = SCAN_WARPS * 32;
 constexpr int VEC_PER_CHUNK = CHUNK_BYTES / 16;
 constexpr int VEC_PER_LANE = VEC_PER_CHUNK / 32;
 constexpr int RING = 128;             // slice-key ring of a streaming warp (a power of two)
@@ -396,15 +395,6 @@ __device__ __forceinline__ void row_barrier(int parity, int threads) {
         asm volatile("bar.sync 1, %0;" ::"r"(threads) : "memory");
     else
         asm volatile("bar.sync 3, %0;" ::"r"(threads) : "memory");
-}
-
-__device__ __forceinline__ int warp_inclusive_scan_i(int v, int lane) {
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int t = __shfl_up_sync(FULL, v, d);
-        if (lane >= d) v += t;
-    }
-    return v;
 }
 
 // Publish a value floor for the row to the other warps of the CTA.
