@@ -448,15 +448,27 @@ def cpu_baseline(shp, budget_s=10.0):
     ref.build()
     nreq = min(shp.B, 8)
     inp = cpu_inputs(shp, nreq)
-    t0 = time.perf_counter()
-    done = 0
-    while (time.perf_counter() - t0) < budget_s:
-        oracle_chain(inp, [done % nreq])
-        done += 1
-    dt = time.perf_counter() - t0
-    return {"value": round(done / dt, 3), "unit": UNIT, "cores": ref.num_threads(), "kind": "oracle",
+
+    def run(budget):
+        t0 = time.perf_counter()
+        done = 0
+        while (time.perf_counter() - t0) < budget:
+            oracle_chain(inp, [done % nreq])
+            done += 1
+        return done, time.perf_counter() - t0
+
+    cores = ref.num_threads()
+    done, dt = run(budget_s)
+    ref.set_num_threads(1)  # the same oracle on one thread, for scale
+    try:
+        done1, dt1 = run(budget_s / 2)
+    finally:
+        ref.set_num_threads(cores)
+    return {"value": round(done / dt, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "value_1_thread": round(done1 / dt1, 3),
             "sample": f"{done} request chains ({nreq} distinct requests of the {shp.name} workload, K={shp.K}, "
-                      f"V={shp.V}) through the whole oracle path, one after another, {dt:.1f} s"}
+                      f"V={shp.V}) through the whole oracle path, one after another, {dt:.1f} s "
+                      f"(and {done1} on one thread in {dt1:.1f} s)"}
 
 
 def run_reference(args, rank, world):
