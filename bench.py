@@ -78,6 +78,22 @@ def _code_only(text):
     return "\n".join(ln for ln in lines if ln)
 
 
+def max_over_ranks(x, dev, world):
+    """The largest of every rank's x (the job ends when its slowest replica does)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(B, world, steps, seconds):
+    """Draft blocks per second of the whole job: every replica runs B requests per step."""
+    return B * world * steps / seconds
+
+
 def kernel_source_sha(kernel):
     h = hashlib.sha256()
     for n in KERNEL_SOURCES[kernel]:
@@ -285,13 +301,9 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), dev, world)
     ms_per_step = ms / args.steps
-    value = shp.B * world * args.steps / (ms / 1e3)
+    value = whole_job_rate(shp.B, world, args.steps, ms / 1e3)
 
     # ---- per-kernel durations: eager steps queued behind a sleep kernel ----
     kern = {}
@@ -406,12 +418,8 @@ def run_e2e(chain, shp, dev, stream, steps, world):
         res_host[1].copy_(chain.out, non_blocking=True)
         res_host[2].copy_(chain.st, non_blocking=True)
         stream.synchronize()
-    dt = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([dt], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dt = float(t.item())
-    return {"value": round(shp.B * world * steps / dt, 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    dt = max_over_ranks(time.perf_counter() - t0, dev, world)
+    return {"value": round(whole_job_rate(shp.B, world, steps, dt), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4)}
 
 
