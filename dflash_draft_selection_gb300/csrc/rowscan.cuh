@@ -160,8 +160,8 @@ struct RowResult {
 };
 
 // ------------------------------------------------------ per-warp streams ----
-// Warp w owns the chunks begin + w, begin + w + 8, ... of its CTA's range:
-// n_w of them.  The issue side runs WSTAGES chunks ahead of the consume side,
+// Warp w owns the chunks begin + w, begin + w + SCAN_WARPS, ... of its CTA's
+// range: n_w of them.  The issue side runs WSTAGES chunks ahead of the consume side,
 // across rows; both walk their position with 32-bit counters (a CTA's range
 // holds far fewer than 2^31 chunks: a device buffer holds fewer than 2^27).
 struct WarpStream {
@@ -863,9 +863,10 @@ __device__ __forceinline__ bool refine_row(ScanSmem &sm, int rp, uint32_t parity
 }
 
 // Completion warp: the CTA's result for its row rrel.  Modes TOPN* first
-// collect the row's best slice keys from the rings; then a bounded wait for the streaming
-// warps' hand-offs (a time-out marks the row bad and stops further waits),
-// merged over the warps; then clear the row's shared state and free the slot.
+// collect the row's best slice keys from the rings; then a bounded wait for
+// the streaming warps' hand-offs (a time-out marks the row bad and stops
+// further waits), merged over the warps; then clear the row's shared state
+// and free the slot.
 template <int R, int MODE, bool BF16>
 __device__ __forceinline__ void take_row(ScanSmem &sm, const ScanGeom &g, int64_t row, RowResult<R> &res, int rrel,
                                          float c, int nsel, uint32_t (&tail)[SCAN_WARPS], bool &aborted, int lane,
@@ -904,9 +905,10 @@ __device__ __forceinline__ void take_row(ScanSmem &sm, const ScanGeom &g, int64_
 // by at least N elements, so every one of the N best elements lies in a slice
 // whose maximum reaches F: re-read those slices (all loads of a list register
 // in flight at once), gather their elements that reach F in shared memory
-// (cursor `ngather`) and rank them.  If the list is full with its last key tied at F (slices tied at
-// F may have been left out), or the gathered elements overflow the buffer,
-// rank every slice of the row instead.  Returns element keys.
+// (cursor `ngather`) and rank them.  If the list is full with its last key
+// tied at F (slices tied at F may have been left out), or the gathered
+// elements overflow the buffer, rank every slice of the row instead.
+// Returns element keys.
 template <int R, bool BF16>
 __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t row, const WarpList<R> &L, int nsel,
                                                     unsigned char *scratch, int *ngather, int lane) {
