@@ -555,6 +555,10 @@ static int check_q(int K, const int32_t *path_tok, const int32_t *cand, const do
  * the accept walk.  tlogits is [B, K+1, V] with row stride ld.  A request with
  * an unusable target row gets status NAN, invalid parameters BAD_PARAMS, bad
  * q as in check_q; such a request commits nothing (accept_len 0, all -1).
+ * margin[b]: the smallest margin of the decisions the request actually took:
+ * the top_p cut of the target rows it used (rows 0..n, n = accept_len), its
+ * accept tests and its draws (as in accept_one); inf for a request with a
+ * nonzero status (its outcome is the status alone).
  */
 void dflash2_ref_verify(const void *tlogits, int dtype, int64_t B, int K, int64_t V, int64_t ld,
                         const int32_t *path_tok, const int32_t *cand_idx, const double *q_sel,
@@ -573,6 +577,7 @@ void dflash2_ref_verify(const void *tlogits, int dtype, int64_t B, int K, int64_
         int32_t *ids = (int32_t *)malloc((size_t)(K + 1) * V * sizeof(int32_t));
         double *pr = (double *)malloc((size_t)(K + 1) * V * sizeof(double));
         dist_t *dists = (dist_t *)malloc((size_t)(K + 1) * sizeof(dist_t));
+        double *row_mg = (double *)malloc((size_t)(K + 1) * sizeof(double));
         if (params_bad(T, tk, tp)) st = REF_ST_BAD_PARAMS;
         for (int t = 0; t <= K && st == REF_ST_OK; t++) {
             const void *row = (const char *)tlogits + (size_t)((b * (K + 1) + t) * ld) * es;
@@ -580,7 +585,7 @@ void dflash2_ref_verify(const void *tlogits, int dtype, int64_t B, int K, int64_
             int64_t n = dflash2_ref_target_dist(row, dtype, V, (float)T, tk, (float)tp,
                                                 ids + (int64_t)t * V, pr + (int64_t)t * V, V, &m1);
             if (n < 0) st = REF_ST_NAN;
-            if (m1 < mg) mg = m1;
+            row_mg[t] = m1;
             dists[t].ids = ids + (int64_t)t * V;
             dists[t].p = pr + (int64_t)t * V;
             dists[t].n = n;
@@ -597,10 +602,13 @@ void dflash2_ref_verify(const void *tlogits, int dtype, int64_t B, int K, int64_
             double m2 = INFINITY;
             accept_one(K, dists, greedy, pt, cd, qs, ps, u_acc + b * K, u_res + b * (K + 1),
                        &accept_len[b], out_tok + b * (K + 1), &m2);
-            if (m2 < mg) mg = m2;
+            mg = m2;
+            for (int t = 0; t <= accept_len[b]; t++)
+                if (row_mg[t] < mg) mg = row_mg[t];
         }
         status[b] = st;
         if (margin) margin[b] = mg;
+        free(row_mg);
         free(ids);
         free(pr);
         free(dists);

@@ -552,3 +552,133 @@ def test_conv_f32_exact_rounding(ref):
         f = np.float32(y[i])
         for nb in (np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(-np.inf))):
             assert abs(Fraction(float(nb)) - ex) >= abs(yv - ex)
+
+
+# ------------------------------------------------- decision margins ----
+# Every GPU parity test excuses a decision whose oracle margin is below 1e-5
+# (the pages accept near-ties: FreeToken PR 857, "Accuracy").  These pins fix
+# the margins themselves to planted distances, so that a margin that came out
+# too small (excusing everything) or too large fails here.
+def _planted_row(V, probs_by_id):
+    """f32 logits whose softmax puts `probs_by_id` on those ids and nothing elsewhere."""
+    z = np.full(V, -np.inf, np.float32)
+    for i, p in probs_by_id.items():
+        z[i] = np.log(p) if p > 0 else -np.inf
+    return z
+
+
+def test_topk16_top_p_margin_is_the_planted_gap(ref):
+    z = _planted_row(64, {7: 0.5, 3: 0.3, 40: 0.15, 12: 0.05})
+    # top_p 0.75: cumulative 0.5 (gap 0.25) then 0.8 (gap 0.05, cut): margin 0.05
+    _, _, _, mg = ref.topk16(torch.tensor(z)[None], params=synth.make_params(1, 1.0, 0, 0.75))
+    assert abs(mg[0] - 0.05) < 1e-6
+    # a cut planted 3e-6 away from a cumulative mass: the row is a near-tie
+    _, U, _, mg = ref.topk16(torch.tensor(z)[None], params=synth.make_params(1, 1.0, 0, 0.8 + 3e-6))
+    assert abs(mg[0] - 3e-6) < 5e-7
+    assert np.isfinite(U[0, :3]).all() and np.isneginf(U[0, 3:]).all()
+    # no top_p decision, no margin
+    for p in (synth.make_params(1, 1.0, 3, 1.0), synth.make_params(1, 0.0, 0, 1.0), None):
+        _, _, _, mg = ref.topk16(torch.tensor(z)[None], params=p)
+        assert np.isinf(mg[0])
+
+
+def test_walk_greedy_margin_is_best_minus_second(ref):
+    idx = np.arange(100, 116, dtype=np.int32)[None]
+    for row, want_slot, want_mg in [([1.0, 1.37, 0.5], 1, 0.37), ([2.0, 2.0, 1.0], 0, 0.0),
+                                    ([0.25], 0, np.inf), ([-1.0, -1.0 + 2 ** -20, -3.0], 1, 2 ** -20)]:
+        S = np.full((1, 1, 16, 16), -np.inf)
+        S[0, 0, 0, :len(row)] = row
+        pt, ps, q, mg = ref.walk(idx, S, np.zeros(1, np.float32), np.zeros((1, 1), np.float32), 1, 1)
+        assert ps[0, 0] == want_slot and pt[0, 0] == 100 + want_slot
+        assert mg[0, 0] == pytest.approx(want_mg, abs=1e-15) if np.isfinite(want_mg) else np.isinf(mg[0, 0])
+
+
+def test_walk_sampled_margin_is_distance_to_nearest_cdf_step(ref):
+    p = np.array([0.1, 0.2, 0.3, 0.4] + [0.0] * 12)
+    S = np.full((1, 1, 16, 16), -np.inf)
+    with np.errstate(divide="ignore"):
+        S[0, 0, 0] = np.log(p)
+    idx = np.arange(100, 116, dtype=np.int32)[None]
+    # CDF steps at 0.1, 0.3, 0.6, 1.0
+    for u, slot, gap in [(0.31, 2, 0.01), (0.5, 2, 0.1), (0.0999, 0, 1e-4), (0.95, 3, 0.05)]:
+        _, ps, _, mg = ref.walk(idx, S, np.ones(1, np.float32), np.array([[u]], np.float32), 1, 1)
+        assert ps[0, 0] == slot
+        assert abs(mg[0, 0] - gap) < 1e-7        # u is an f32: |u - f32(u)| < 3e-9
+
+
+def test_walk_sampled_fallback_takes_the_last_positive_slot(ref):
+    """u = 1 crosses no CDF step (the running sum reaches the total exactly, never
+    above it): the draw falls back to the last slot with q > 0, skipping the
+    -inf slots after it."""
+    p = np.array([0.1, 0.2, 0.0, 0.3, 0.4] + [0.0] * 11)
+    S = np.full((1, 1, 16, 16), -np.inf)
+    with np.errstate(divide="ignore"):
+        S[0, 0, 0] = np.log(p)
+    idx = np.arange(100, 116, dtype=np.int32)[None]
+    _, ps, q, _ = ref.walk(idx, S, np.ones(1, np.float32), np.ones((1, 1), np.float32), 1, 1)
+    assert ps[0, 0] == 4 and q[0, 0, 4] > 0 and np.all(q[0, 0, 5:] == 0)
+
+
+def _verify_case(ref, rows, cands, qs, path, slot, u_acc, u_res, top_k=0, top_p=1.0, trusted=False, V=64):
+    """One sampled request (T = 1) with planted target rows (dicts id -> p) and q rows."""
+    K = len(path)
+    y = np.stack([_planted_row(V, r) for r in rows])
+    cand = np.zeros((1, K, 16), np.int32)
+    q = np.zeros((1, K, 16))
+    for t in range(K):
+        c = list(cands[t]) + [x for x in range(V) if x not in cands[t]][:16 - len(cands[t])]
+        cand[0, t] = c
+        q[0, t, :len(qs[t])] = qs[t]
+    params = synth.make_params(1, 1.0, top_k, top_p)
+    return ref.verify(torch.tensor(y), np.array([path], np.int32), cand, q, np.array([slot], np.int32), params,
+                      np.array([u_acc], np.float32), np.array([u_res], np.float32), 1, K, trusted=trusted)
+
+
+def test_verify_margin_of_an_accept_test_and_of_a_draw(ref):
+    rows = [{5: 0.6, 9: 0.4}, {3: 0.4, 12: 0.6}]
+    # accept: u q = 0.7 * 0.5 = 0.35 < p = 0.4 (gap 0.05); bonus draw over ids 3, 12 at u = 0.5:
+    # CDF steps 0.4 (gap 0.1) and 1.0 -> token 12
+    acc, out, st, mg = _verify_case(ref, rows, [[9, 5]], [[0.5, 0.5]], [9], [0], [0.7], [0.3, 0.5], top_k=2)
+    assert st[0] == 0 and acc[0] == 1 and out[0].tolist() == [9, 12]
+    assert abs(mg[0] - 0.05) < 1e-6
+    # reject: 0.9 * 0.5 = 0.45 >= 0.4 (gap 0.05); the residual max(0, p - q) is 0.1 on token 5 only,
+    # drawn at u = 0.99: relative gap 1 - 0.99 = 0.01 binds
+    acc, out, st, mg = _verify_case(ref, rows, [[9, 5]], [[0.5, 0.5]], [9], [0], [0.9], [0.99, 0.5], top_k=2)
+    assert acc[0] == 0 and out[0].tolist() == [5, -1]
+    assert abs(mg[0] - 0.01) < 1e-6
+
+
+def test_verify_margin_ignores_rows_the_request_never_used(ref):
+    """A top_p cut within 1e-8 of a cumulative mass on the bonus row must not
+    excuse a request that stopped at position 0."""
+    rows = [{5: 0.6, 9: 0.4}, {5: 0.6, 9: 0.4}, {2: 0.7, 8: 0.3}]
+    acc, out, st, mg = _verify_case(ref, rows, [[9, 5], [5, 9]], [[0.5, 0.5], [0.5, 0.5]], [9, 5], [0, 0],
+                                    [0.9, 0.1], [0.5, 0.5, 0.5], top_p=0.7)
+    assert acc[0] == 0 and out[0, 0] == 5
+    # used: row 0's cut (cumulative 0.6, 1.0 against 0.7: gap 0.1), the accept test (0.05), the draw
+    assert abs(mg[0] - 0.05) < 1e-6
+    # the same bonus row is a near-tie once the request reaches it
+    acc, out, st, mg = _verify_case(ref, rows, [[9, 5], [5, 9]], [[0.5, 0.5], [0.5, 0.5]], [9, 5], [0, 0],
+                                    [0.1, 0.1], [0.5, 0.5, 0.5], top_p=0.7)
+    assert acc[0] == 2 and mg[0] < 1e-6
+
+
+def test_verify_zero_residual_draws_from_p(ref):
+    """A trusted q that is >= p on all of p's support (here q sums to 2.2) leaves a
+    zero residual: the corrected token is drawn from p itself, by inverse CDF
+    over ascending token ids.  p = {10: .3, 25: .2, 40: .5} has CDF steps .3,
+    .5, 1; q normalised would put them at .318, .591, 1, so the two laws give
+    different tokens at u = .31 and u = .55."""
+    rows = [{40: 0.5, 10: 0.3, 25: 0.2}, {1: 1.0}]
+    for u, want in [(0.31, 25), (0.55, 40), (0.2, 10), (0.9, 40)]:
+        acc, out, st, _ = _verify_case(ref, rows, [[40, 10, 25]], [[0.9, 0.7, 0.6]], [40], [0], [0.7], [u, 0.5],
+                                       top_k=3, trusted=True)
+        assert st[0] == 0 and acc[0] == 0 and out[0, 0] == want, (u, out[0])
+
+
+def test_verify_draw_fallback_takes_the_last_positive_token(ref):
+    """u = 1 crosses no CDF step: the bonus draw falls back to the largest
+    token id with positive probability."""
+    rows = [{5: 0.6, 9: 0.4}, {3: 0.4, 12: 0.6, 30: 0.0}]
+    acc, out, st, _ = _verify_case(ref, rows, [[9, 5]], [[0.5, 0.5]], [9], [0], [0.1], [0.5, 1.0], top_k=3)
+    assert acc[0] == 1 and out[0].tolist() == [9, 12]
