@@ -17,3 +17,14 @@ def ref():
     import oracle
     oracle.build()
     return oracle
+
+
+def pytest_terminal_summary(terminalreporter):
+    from tests import _parity
+    if _parity.LOG:
+        exc = sum(e for _, e, _ in _parity.LOG)
+        dec = sum(d for _, _, d in _parity.LOG)
+        terminalreporter.write_line(f"near-tie decisions excused: {exc} of {dec} compared in {len(_parity.LOG)} checks")
+        for what, e, d in _parity.LOG:
+            if e:
+                terminalreporter.write_line(f"  {what}: {e} of {d}")

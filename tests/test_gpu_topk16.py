@@ -1,10 +1,14 @@
-"""dflash2_topk16 against the oracle (bit-exact ids, U and lse within 1e-4 rel)."""
+"""dflash2_topk16 against the oracle: bit-exact ids; U and lse within 1e-4 rel,
+except on a row whose top_p cut is within 1e-5 of a cumulative mass, where
+the GPU's cut may move by one token and its U must be that cut's filtered
+distribution (tests/_parity.py; at most 1% of the rows)."""
 import numpy as np
 import pytest
 import torch
 
 import dflash_draft_selection_gb300 as d2
 from dflash_draft_selection_gb300 import synth
+from tests import _parity
 from tests._util import MARGIN, assert_close, cuda_or_skip, padded, params_np
 
 pytestmark = pytest.mark.gpu
@@ -19,15 +23,14 @@ def run_both(ref, z, params=None, rpp=1, V=None):
     idx, U, lse = d2.topk16(zg, params=pg, rows_per_param=rpp, V=Vv)
     torch.cuda.synchronize()
     r_idx, r_U, r_lse, r_mg = ref.topk16(z, params=params, rows_per_param=rpp, V=Vv, ld=z.shape[1])
-    return idx.cpu().numpy(), U.cpu().numpy(), lse.cpu().numpy(), r_idx, r_U, r_lse, r_mg
+    prow = synth.make_params(z.shape[0], 0.0, 0, 1.0) if params is None else np.repeat(params, rpp)[:z.shape[0]]
+    return z, prow, idx.cpu().numpy(), U.cpu().numpy(), lse.cpu().numpy(), r_idx, r_U, r_lse, r_mg
 
 
 def compare(res, what):
-    idx, U, lse, r_idx, r_U, r_lse, r_mg = res
-    np.testing.assert_array_equal(idx, r_idx, err_msg=what)
-    ok = r_mg >= MARGIN  # rows whose top_p decision is within rounding of the threshold are exempt
-    assert_close(U[ok], r_U[ok], what=what + " U")
-    assert_close(lse[ok], r_lse[ok], what=what + " lse")
+    ex = _parity.Excused()
+    _parity.topk_compare(*res, ex, what=what)
+    ex.check_bound(what=what)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -110,13 +113,13 @@ def test_bad_rows_and_params(ref):
     z[1, 9] = float("inf")
     z[2, :] = float("-inf")
     z[3, :690] = float("-inf")
-    idx, U, lse, r_idx, r_U, r_lse, _ = run_both(ref, z)
+    _, _, idx, U, lse, r_idx, r_U, r_lse, _ = run_both(ref, z)
     np.testing.assert_array_equal(idx, r_idx)
     assert_close(U, r_U)
     p = params_np(6, 1.0, 10, 1.0)
     p["top_p"][4] = 0.0                  # invalid
     p["temperature"][5] = -1.0           # invalid
-    idx, U, lse, r_idx, r_U, r_lse, _ = run_both(ref, z, params=p)
+    _, _, idx, U, lse, r_idx, r_U, r_lse, _ = run_both(ref, z, params=p)
     np.testing.assert_array_equal(idx, r_idx)
     assert np.all(idx[4:] == -1) and np.all(np.isnan(U[4:]))
 
@@ -141,8 +144,8 @@ def test_empty_and_invalid(ref):
 
 
 @pytest.mark.parametrize("name", ["27b_greedy", "27b_sampled", "stress"])
-def test_full_size_sampled_rows(ref, name):
-    """The full workload in the bench's launch configuration; a sample of rows checked one by one."""
+def test_full_size_all_rows(ref, name):
+    """The full workload in the bench's launch configuration, every row checked against the oracle."""
     dev = cuda_or_skip()
     shp = synth.WORKLOADS[name]
     g = torch.Generator(device=dev).manual_seed(shp.seed)
@@ -154,18 +157,16 @@ def test_full_size_sampled_rows(ref, name):
     pg = d2.sampling_params(p["temperature"], p["top_k"], p["top_p"], device=dev)
     idx, U, lse = d2.topk16(z, params=pg if shp.temperature > 0 else None, rows_per_param=shp.K)
     torch.cuda.synchronize()
-    pick = torch.randperm(rows, generator=torch.Generator().manual_seed(0))[:24].sort().values
-    if shp.dup_frac:  # include rows with a duplicated maximum
+    if shp.dup_frac:  # the rows with a duplicated maximum are among them
         zz = z.float()
         mx = zz.max(dim=1, keepdim=True).values
-        dup = ((zz == mx).sum(dim=1) > 1).nonzero().flatten()[:8].cpu()
-        assert dup.numel() > 0
-        pick = torch.cat([pick, dup]).unique()
-    zs = z[pick.to(dev)].cpu()
-    pr = None if shp.temperature == 0 else np.repeat(p[:1], len(pick))
-    r_idx, r_U, r_lse, r_mg = ref.topk16(zs, params=pr)
-    np.testing.assert_array_equal(idx.cpu().numpy()[pick.numpy()], r_idx)
-    ok = r_mg >= MARGIN
-    assert_close(U.cpu().numpy()[pick.numpy()][ok], r_U[ok], what=name + " U")
-    assert_close(lse.cpu().numpy()[pick.numpy()][ok], r_lse[ok], what=name + " lse")
+        assert ((zz == mx).sum(dim=1) > 1).any()
+    zc = z.cpu()   # every row, checked one by one against the oracle
+    pr = None if shp.temperature == 0 else p
+    r_idx, r_U, r_lse, r_mg = ref.topk16(zc, params=pr, rows_per_param=shp.K)
+    prow = synth.make_params(rows, 0.0, 0, 1.0) if pr is None else np.repeat(p, shp.K)
+    ex = _parity.Excused()
+    _parity.topk_compare(zc, prow, idx.cpu().numpy(), U.cpu().numpy(), lse.cpu().numpy(), r_idx, r_U, r_lse, r_mg,
+                         ex, what=name)
+    ex.check_bound(what=name)
     assert d2.device_error() == 0

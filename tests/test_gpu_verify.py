@@ -1,12 +1,15 @@
-"""dflash2_verify against the oracle: bit-exact accept counts, tokens and status
-(except requests whose oracle decision margin is below 1e-5), plus a Monte Carlo
-of the committed-token marginals on the GPU."""
+"""dflash2_verify against the oracle: bit-exact statuses, accept counts and
+tokens, except at a decision whose oracle margin is below 1e-5, which must be a
+valid outcome of a near-tie and after which the oracle goes on with the GPU's
+decision forced (tests/_parity.py; at most 1% of the decisions excused); plus
+a Monte Carlo of the committed-token marginals on the GPU."""
 import numpy as np
 import pytest
 import torch
 
 import dflash_draft_selection_gb300 as d2
 from dflash_draft_selection_gb300 import synth
+from tests import _parity
 from tests._util import MARGIN, cuda_or_skip, padded, params_np
 
 pytestmark = pytest.mark.gpu
@@ -35,13 +38,11 @@ def run_gpu_verify(inp, cand, pt, ps, q, params, B, K, trusted=False, V=None):
 def check(ref, inp, cand, pt, ps, q, params, B, K, trusted=False):
     acc, out, st = run_gpu_verify(inp, cand, pt, ps, q, params, B, K, trusted)
     # the oracle sees the same f32 q the GPU sees
-    r_acc, r_out, r_st, r_mg = ref.verify(inp.target_logits, pt, cand, q.astype(np.float32).astype(np.float64),
-                                          ps, params, inp.u_acc, inp.u_res, B, K, trusted=trusted)
-    ok = r_mg >= MARGIN
-    np.testing.assert_array_equal(st, r_st)
-    np.testing.assert_array_equal(acc[ok], r_acc[ok])
-    np.testing.assert_array_equal(out[ok], r_out[ok])
-    return acc, ok
+    ex = _parity.Excused()
+    _parity.verify_compare(ref, inp.target_logits, pt, cand, q.astype(np.float32), ps, params, inp.u_acc.numpy(),
+                           inp.u_res.numpy(), acc, out, st, ex, trusted=trusted)
+    ex.check_bound(what="verify")
+    return acc, ex
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -61,8 +62,8 @@ def test_greedy_prefix(ref, dtype, V):
     ps = np.zeros((B, K), np.int32)
     q = np.zeros((B, K, 16))
     q[..., 0] = 1.0
-    acc, ok = check(ref, inp, cand, pt, ps, q, None, B, K)
-    assert ok.all()
+    acc, ex = check(ref, inp, cand, pt, ps, q, None, B, K)
+    assert ex.excused == 0
     assert acc.tolist() == [0, 1, 2, 3, 4, 5, 6, 7, 7]
 
 
@@ -74,8 +75,7 @@ def test_sampled_parity(ref, seed, T, k, p):
                             target_noise=1.0)
     inp = synth.make_inputs(shp, with_conv=False)
     cand, pt, ps, q = oracle_walk_inputs(ref, inp, B, K)
-    acc, ok = check(ref, inp, cand, pt, ps, q, inp.params, B, K)
-    assert ok.mean() > 0.8
+    check(ref, inp, cand, pt, ps, q, inp.params, B, K)
 
 
 def test_mixed_greedy_and_sampled(ref):
@@ -189,14 +189,9 @@ def test_full_size_sampled_requests(ref, name):
     acc, out, st = d2.verify(inp.target_logits, pt, cand.view(B, K, 16), q, ps, params=pg,
                              u_acc=inp.u_acc if pg is not None else None, u_res=inp.u_res if pg is not None else None)
     torch.cuda.synchronize()
-    pick = np.array([0, 5, 17, 31, 42, 63])
-    tl = inp.target_logits.view(B, K + 1, V)[pick].reshape(-1, V).cpu()
-    r_acc, r_out, r_st, r_mg = ref.verify(tl, pt.cpu()[pick], cand.view(B, K, 16).cpu()[pick],
-                                          q.cpu().double()[pick], ps.cpu()[pick],
-                                          None if params is None else params[pick], inp.u_acc.cpu()[pick],
-                                          inp.u_res.cpu()[pick], len(pick), K)
-    ok = r_mg >= MARGIN
-    np.testing.assert_array_equal(st.cpu().numpy()[pick], r_st)
-    np.testing.assert_array_equal(acc.cpu().numpy()[pick][ok], r_acc[ok])
-    np.testing.assert_array_equal(out.cpu().numpy()[pick][ok], r_out[ok])
+    ex = _parity.Excused()   # every request
+    _parity.verify_compare(ref, inp.target_logits.cpu(), pt.cpu().numpy(), cand.view(B, K, 16).cpu().numpy(),
+                           q.cpu().numpy(), ps.cpu().numpy(), params, inp.u_acc.cpu().numpy(), inp.u_res.cpu().numpy(),
+                           acc.cpu().numpy(), out.cpu().numpy(), st.cpu().numpy(), ex, what=name)
+    ex.check_bound(what=name)
     assert d2.device_error() == 0

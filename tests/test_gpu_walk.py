@@ -1,11 +1,14 @@
-"""dflash2_pair_score_walk against the oracle: scores within 1e-4 rel, paths and
-slots bit-exact up to the first step whose oracle margin is below 1e-5."""
+"""dflash2_pair_score_walk against the oracle: scores within 1e-4 rel; paths and
+slots bit-exact, except at a sampled step whose oracle margin is below 1e-5,
+where the GPU's draw must be a neighbour of the CDF step and the comparison
+goes on from it (at most 1% of the steps excused)."""
 import numpy as np
 import pytest
 import torch
 
 import dflash_draft_selection_gb300 as d2
-from tests._util import MARGIN, assert_close, cuda_or_skip
+from tests import _parity
+from tests._util import assert_close, cuda_or_skip
 
 pytestmark = pytest.mark.gpu
 
@@ -37,15 +40,12 @@ def run(ref, B, K, V, D, seed, T=0.0, dtype=torch.bfloat16, scale=0.25, mutate=N
     r_S = ref.pair_scores(idx, U.astype(np.float64), last, A, Bt, gate.double().numpy(), B, K)
     assert_close(S.cpu().numpy(), r_S, what="scores")
     Tn = np.full(B, T, np.float32)
-    # the walk: oracle over the GPU's own scores, so only the walk is compared
-    r_pt, r_ps, r_q, r_mg = ref.walk(idx, S.cpu().double().numpy(), Tn, u.numpy(), B, K)
+    # the walk: the oracle over the GPU's own scores, so only the walk is compared
     pt, ps, q = pt.cpu().numpy(), ps.cpu().numpy(), q.cpu().numpy()
-    for b in range(B):
-        for t in range(K):
-            if r_mg[b, t] < MARGIN:
-                break
-            assert pt[b, t] == r_pt[b, t] and ps[b, t] == r_ps[b, t], (b, t)
-            assert_close(q[b, t], r_q[b, t], what="q")
+    ex = _parity.Excused()
+    _parity.walk_compare(ref, idx, S.cpu().double().numpy(), Tn, u.numpy(), pt, ps, q, ex)
+    ex.check_bound(what="walk")
+    r_mg = ref.walk(idx, S.cpu().double().numpy(), Tn, u.numpy(), B, K)[3]
     return pt, ps, q, r_mg
 
 
