@@ -15,5 +15,6 @@ from .binding import (  # noqa: F401
     pair_score_walk,
     sampling_params,
     topk16,
+    topk16_noalloc,
     verify,
 )

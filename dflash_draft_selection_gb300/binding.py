@@ -49,6 +49,7 @@ def load_library():
         L.dflash2_topk16_workspace_bytes.argtypes = [i64]
         L.dflash2_topk16_workspace_bytes.restype = sz
         L.dflash2_topk16.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp, sz, vp]
+        L.dflash2_topk16_noalloc.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp]
         L.dflash2_ctx_gate.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp]
         L.dflash2_pair_score_walk_workspace_bytes.argtypes = [i64]
         L.dflash2_pair_score_walk_workspace_bytes.restype = sz
@@ -62,8 +63,8 @@ def load_library():
         L.dflash2_status_string.argtypes = [i32]
         L.dflash2_status_string.restype = ctypes.c_char_p
         L.dflash2_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
-        for fn in ("dflash2_topk16", "dflash2_ctx_gate", "dflash2_pair_score_walk", "dflash2_verify",
-                   "dflash2_conv2tap", "dflash2_device_error"):
+        for fn in ("dflash2_topk16", "dflash2_topk16_noalloc", "dflash2_ctx_gate", "dflash2_pair_score_walk",
+                   "dflash2_verify", "dflash2_conv2tap", "dflash2_device_error"):
             getattr(L, fn).restype = i32
         _lib = L
         return _lib
@@ -167,6 +168,26 @@ def topk16(logits: torch.Tensor, params=None, rows_per_param: int = 1, V: int | 
     _check("dflash2_topk16", L.dflash2_topk16(_ptr(logits), _dtype(logits), rows, V, ld, _ptr(p), rows_per_param,
                                               _ptr(cand_idx), _ptr(cand_U), _ptr(lse), ws.ptr(), ws.nbytes,
                                               _stream(dev)))
+    return cand_idx, cand_U, lse
+
+
+def topk16_noalloc(logits: torch.Tensor, params=None, rows_per_param: int = 1, V: int | None = None, out=None):
+    """dflash2_topk16_noalloc: topk16 with the library's own fixed scratch.  Returns (cand_idx, cand_U, lse)."""
+    L = load_library()
+    _need_cuda(logits)
+    assert logits.dim() == 2 and logits.stride(1) == 1
+    rows, ld = logits.shape[0], logits.stride(0)
+    V = logits.shape[1] if V is None else V
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(rows, NC, dtype=torch.int32, device=dev),
+               torch.empty(rows, NC, dtype=torch.float32, device=dev),
+               torch.empty(rows, dtype=torch.float32, device=dev))
+    cand_idx, cand_U, lse = out
+    p = _params_from(params, dev)
+    _check("dflash2_topk16_noalloc",
+           L.dflash2_topk16_noalloc(_ptr(logits), _dtype(logits), rows, V, ld, _ptr(p), rows_per_param,
+                                    _ptr(cand_idx), _ptr(cand_U), _ptr(lse), _stream(dev)))
     return cand_idx, cand_U, lse
 
 

@@ -164,10 +164,12 @@ extern "C" size_t dflash2_topk16_workspace_bytes(int64_t rows) {
     return scan_ws_bytes(rows);
 }
 
-extern "C" dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
-                                         int64_t ld, const dflash2_sampling *params,
-                                         int64_t rows_per_param, int32_t *cand_idx, float *cand_U,
-                                         float *lse, void *ws, size_t ws_bytes, dflash2_stream stream) {
+// Argument checks, then (with clear_tickets) zeroing of the rows' tickets in
+// ws on `s`, then the launch.
+static dflash2_status topk16_call(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V, int64_t ld,
+                                  const dflash2_sampling *params, int64_t rows_per_param, int32_t *cand_idx,
+                                  float *cand_U, float *lse, void *ws, size_t ws_bytes, bool clear_tickets,
+                                  cudaStream_t s) {
     if (!dtype_ok(dt) || rows < 0 || V < NC || V >= (int64_t(1) << 31) || ld < V || rows_per_param < 1)
         return DFLASH2_ERR_INVALID_ARG;
     const int es = esize(dt);
@@ -180,10 +182,72 @@ extern "C" dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, i
     if (ws_bytes < scan_ws_bytes(rows)) return DFLASH2_ERR_WORKSPACE;
     const ScanGeom g = make_geom(logits, ld, es, V, rows, params, rows_per_param);
     const ScanWs sw = scan_ws_at(ws, rows);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (clear_tickets && cudaMemsetAsync(sw.tickets, 0, static_cast<size_t>(rows) * sizeof(int32_t), s) != cudaSuccess)
+        return DFLASH2_ERR_CUDA;
     if (params == nullptr)
         return dt == DFLASH2_BF16 ? launch_topk16<false, true>(g, sw, cand_idx, cand_U, lse, s)
                                   : launch_topk16<false, false>(g, sw, cand_idx, cand_U, lse, s);
     return dt == DFLASH2_BF16 ? launch_topk16<true, true>(g, sw, cand_idx, cand_U, lse, s)
                               : launch_topk16<true, false>(g, sw, cand_idx, cand_U, lse, s);
+}
+
+extern "C" dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
+                                         int64_t ld, const dflash2_sampling *params,
+                                         int64_t rows_per_param, int32_t *cand_idx, float *cand_U,
+                                         float *lse, void *ws, size_t ws_bytes, dflash2_stream stream) {
+    return topk16_call(logits, dt, rows, V, ld, params, rows_per_param, cand_idx, cand_U, lse, ws, ws_bytes, false,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// dflash2_topk16_noalloc: the same call for callers that cannot hand this
+// library any device memory of their own.  Its scratch -- one ticket per row
+// and the partial records of rows split over several CTAs -- is a fixed array
+// in the library's own device memory instead of a workspace.
+namespace dfl {
+
+constexpr int64_t TOPK_NOALLOC_MAX_ROWS = DFLASH2_TOPK16_NOALLOC_MAX_ROWS;
+constexpr size_t TOPK_NOALLOC_BYTES =
+    (TOPK_NOALLOC_MAX_ROWS * sizeof(int32_t) + 255) / 256 * 256 + static_cast<size_t>(2 * MAX_SCAN_GRID) * sizeof(PartRec);
+
+// Every GPU that loads the library holds this array (about 1.1 MB) until the
+// process exits.  All calls share it.
+static __device__ __align__(256) unsigned char g_topk_noalloc_ws[TOPK_NOALLOC_BYTES];
+
+// Device address of the array on the current device, looked up once per
+// device with that device current (in host code the array's name is only a
+// host-side stand-in).  NULL if the lookup fails.
+static void *topk_noalloc_ws() {
+    static void *addr[64] = {nullptr};
+    static std::mutex mu;
+    const int dev = current_device();
+    if (dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_topk_noalloc_ws) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace dfl
+
+extern "C" dflash2_status dflash2_topk16_noalloc(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
+                                                 int64_t ld, const dflash2_sampling *params, int64_t rows_per_param,
+                                                 int32_t *cand_idx, float *cand_U, float *lse,
+                                                 dflash2_stream stream) {
+    if (rows > dfl::TOPK_NOALLOC_MAX_ROWS) return DFLASH2_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (rows <= 0)  // argument errors and the empty batch, reported as the workspace call does
+        return topk16_call(logits, dt, rows, V, ld, params, rows_per_param, cand_idx, cand_U, lse, nullptr, 0,
+                           false, s);
+    void *ws = dfl::topk_noalloc_ws();
+    if (!ws) return DFLASH2_ERR_CUDA;
+    // The tickets of the call's rows must start at zero.  A call leaves them
+    // zero again, but one cut short (a launch error, or a kernel that gave up
+    // on a bounded wait) may not, so every call clears them first.  The
+    // partial records are written before they are read and need no clearing.
+    return topk16_call(logits, dt, rows, V, ld, params, rows_per_param, cand_idx, cand_U, lse, ws,
+                       dfl::TOPK_NOALLOC_BYTES, true, s);
 }

@@ -435,54 +435,3 @@ extern "C" dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const in
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return tdt == DFLASH2_BF16 ? launch_walk<true>(a, s) : launch_walk<false>(a, s);
 }
-
-// ---------------------------------------------------------------------------
-// dflash2_pair_score_walk_noalloc: the same call for callers that cannot hand
-// this library any device memory of their own.  The per-request tickets live
-// in a fixed array in the library's device memory instead of a workspace.
-namespace dfl {
-
-constexpr int64_t WALK_NOALLOC_MAX_B = DFLASH2_WALK_NOALLOC_MAX_B;
-
-// One ticket per request; every GPU that loads the library holds this array
-// (64 KB) until the process exits.  All calls share it.
-static __device__ __align__(256) int32_t g_walk_noalloc_tickets[WALK_NOALLOC_MAX_B];
-
-// Device address of the ticket array on the current device, looked up once
-// per device with that device current.  In host code the array's name is
-// only a host-side stand-in, so the address must come from the runtime.
-static int32_t *walk_noalloc_tickets() {
-    static int32_t *addr[64] = {nullptr};
-    static std::mutex mu;
-    const int dev = current_device();
-    if (dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_walk_noalloc_tickets) != cudaSuccess) return nullptr;
-        addr[dev] = static_cast<int32_t *>(p);
-    }
-    return addr[dev];
-}
-
-}  // namespace dfl
-
-extern "C" dflash2_status dflash2_pair_score_walk_noalloc(
-    int64_t B, int32_t K, const int32_t *cand_idx, const float *cand_U, const int32_t *last_tok, const void *A,
-    const void *Bt, dflash2_dtype tdt, int64_t V, int32_t D, const float *gate, const dflash2_sampling *params,
-    const float *u_walk, int32_t *path_tok, int32_t *path_slot, float *q_sel, float *scores,
-    dflash2_stream stream) {
-    if (B > dfl::WALK_NOALLOC_MAX_B) return DFLASH2_ERR_WORKSPACE;
-    if (B <= 0)
-        return dflash2_pair_score_walk(B, K, cand_idx, cand_U, last_tok, A, Bt, tdt, V, D, gate, params, u_walk,
-                                       path_tok, path_slot, q_sel, scores, nullptr, 0, stream);
-    int32_t *tickets = dfl::walk_noalloc_tickets();
-    if (!tickets) return DFLASH2_ERR_CUDA;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    // The tickets must start at zero: clear this call's share of the array.
-    if (cudaMemsetAsync(tickets, 0, static_cast<size_t>(B) * sizeof(int32_t), s) != cudaSuccess)
-        return DFLASH2_ERR_CUDA;
-    return dflash2_pair_score_walk(B, K, cand_idx, cand_U, last_tok, A, Bt, tdt, V, D, gate, params, u_walk,
-                                   path_tok, path_slot, q_sel, scores, tickets,
-                                   sizeof(int32_t) * static_cast<size_t>(dfl::WALK_NOALLOC_MAX_B), stream);
-}

@@ -65,7 +65,9 @@ enum {
 };
 
 #define DFLASH2_NC 16        /* candidates per draft position ([P] item 1) */
-#define DFLASH2_MAX_K 15     /* drafted positions: 1 .. block_size - 1 with block_size <= 16 ([F] Refused at startup) */
+#define DFLASH2_MAX_K 15     /* drafted positions: [F] Details refuses k outside 1 .. block_size - 1; the pages
+                                set no bound on block_size, and the cap of 15 (block_size <= 16) is this
+                                library's own limit, not a number the pages print */
 #define DFLASH2_MAX_TOPK 64  /* largest top_k a filtered row may use */
 
 /*
@@ -112,6 +114,34 @@ dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows
                               int64_t ld, const dflash2_sampling *params, int64_t rows_per_param,
                               int32_t *cand_idx, float *cand_U, float *lse, void *ws,
                               size_t ws_bytes, dflash2_stream stream);
+
+/*
+ * dflash2_topk16_noalloc -- no counterpart on the pages: an addition of this
+ * library.  The same computation, arguments and argument errors as
+ * dflash2_topk16, without the workspace, for callers that cannot give this
+ * library device memory: a plugin, or an engine whose memory pool owns all
+ * device memory and hands no scratch to the code it calls, or code that may
+ * not call an allocator at the point where the drafter's rows are reduced.
+ * The scratch (one ticket per row, and the partial records of rows that the
+ * kernel splits over several CTAs) is a fixed array in the library's own
+ * device memory, sized for DFLASH2_TOPK16_NOALLOC_MAX_ROWS rows (about 1.1 MB),
+ * held by every GPU that loads the library until the process exits.
+ *   - rows > DFLASH2_TOPK16_NOALLOC_MAX_ROWS returns DFLASH2_ERR_WORKSPACE and
+ *     launches nothing.
+ *   - Nothing is allocated.  The tickets must start at zero: each call clears
+ *     those of its rows (cudaMemsetAsync on `stream`) before the kernel.  The
+ *     partial records are written before they are read.
+ *   - The first call on a device looks up the array's device address (once,
+ *     with that device current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array: calls that overlap on the GPU (on
+ *     different streams, or from different threads) race on it and their
+ *     outputs are undefined.  Issue them on one stream.
+ */
+#define DFLASH2_TOPK16_NOALLOC_MAX_ROWS 16384
+dflash2_status dflash2_topk16_noalloc(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
+                                      int64_t ld, const dflash2_sampling *params, int64_t rows_per_param,
+                                      int32_t *cand_idx, float *cand_U, float *lse, dflash2_stream stream);
 
 /*
  * dflash2_ctx_gate -- [P] item 1 "context gate" of the bilinear selector,
@@ -163,39 +193,6 @@ dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand
                                        int32_t *path_tok, int32_t *path_slot, float *q_sel,
                                        float *scores, void *ws, size_t ws_bytes,
                                        dflash2_stream stream);
-
-/*
- * dflash2_pair_score_walk_noalloc -- no counterpart on the pages: an addition
- * of this library.  The same computation and arguments as
- * dflash2_pair_score_walk, without the workspace, for callers that cannot
- * give this library device memory: for example a plugin or an engine whose
- * memory pool owns all device memory and offers no scratch to the code it
- * calls, or code that may not call an allocator at the point where the
- * selector runs.  The scratch (one ticket per request) is a fixed array in
- * the library's own device memory, DFLASH2_WALK_NOALLOC_MAX_B tickets (64 KB)
- * held by every GPU that loads the library until the process exits.
- *   - B > DFLASH2_WALK_NOALLOC_MAX_B returns DFLASH2_ERR_WORKSPACE and
- *     launches nothing; other argument errors are those of
- *     dflash2_pair_score_walk.
- *   - Nothing is allocated: each call clears its share of the array
- *     (cudaMemsetAsync on `stream`) and then launches the kernel.
- *   - The first call on a device looks up the array's device address (once,
- *     with that device current); make that first call before any stream
- *     capture.
- *   - All calls share the one array.  The walk keeps each request's state in
- *     the shared memory of the request's thread-block cluster and does not
- *     read the tickets, so calls that overlap on the GPU only race on
- *     clearing the array, which does not change any result.
- */
-#define DFLASH2_WALK_NOALLOC_MAX_B 16384
-dflash2_status dflash2_pair_score_walk_noalloc(int64_t B, int32_t K, const int32_t *cand_idx,
-                                               const float *cand_U, const int32_t *last_tok,
-                                               const void *A, const void *Bt, dflash2_dtype tdt,
-                                               int64_t V, int32_t D, const float *gate,
-                                               const dflash2_sampling *params,
-                                               const float *u_walk, int32_t *path_tok,
-                                               int32_t *path_slot, float *q_sel, float *scores,
-                                               dflash2_stream stream);
 
 /*
  * dflash2_verify -- [F] Sampled verify (accept with min(1, p/q); on a reject
