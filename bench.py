@@ -199,7 +199,6 @@ class Chain:
         self.q, self.S = e(B, K, 16), e(B, K, 16, 16)
         self.acc, self.out, self.st = e(B, dt=torch.int32), e(B, K + 1, dt=torch.int32), e(B, dt=torch.int32)
         self.ws_topk = d2.Workspace.for_topk16(B * K, dev)
-        self.ws_walk = d2.Workspace.for_walk(B, dev)
         self.ws_verify = d2.Workspace.for_verify(B, K, dev)
 
     def call(self, which, inp):
@@ -213,7 +212,7 @@ class Chain:
         elif which == "k_pair_score_walk":
             d2.pair_score_walk(self.cand.view(B, K, 16), self.U.view(B, K, 16), inp.last_tok, self.A, self.Bt,
                                self.gate.view(B, K, -1), params=pg, u_walk=inp.u_walk if self.sampled else None,
-                               ws=self.ws_walk, out=(self.pt, self.ps, self.q, self.S))
+                               out=(self.pt, self.ps, self.q, self.S))
         else:
             d2.verify(inp.target_logits, self.pt, self.cand.view(B, K, 16), self.q, self.ps, params=pg,
                       u_acc=inp.u_acc if self.sampled else None, u_res=inp.u_res if self.sampled else None,

@@ -51,10 +51,8 @@ def load_library():
         L.dflash2_topk16.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp, sz, vp]
         L.dflash2_topk16_noalloc.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp]
         L.dflash2_ctx_gate.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp]
-        L.dflash2_pair_score_walk_workspace_bytes.argtypes = [i64]
-        L.dflash2_pair_score_walk_workspace_bytes.restype = sz
         L.dflash2_pair_score_walk.argtypes = [i64, i32, vp, vp, vp, vp, vp, i32, i64, i32, vp, vp, vp, vp, vp,
-                                              vp, vp, vp, sz, vp]
+                                              vp, vp, vp]
         L.dflash2_verify_workspace_bytes.argtypes = [i64, i32]
         L.dflash2_verify_workspace_bytes.restype = sz
         L.dflash2_verify.argtypes = [vp, i32, i64, i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, u32, vp, vp, vp,
@@ -140,10 +138,6 @@ class Workspace:
         return Workspace(load_library().dflash2_topk16_workspace_bytes(rows), device)
 
     @staticmethod
-    def for_walk(B: int, device="cuda") -> "Workspace":
-        return Workspace(load_library().dflash2_pair_score_walk_workspace_bytes(B), device)
-
-    @staticmethod
     def for_verify(B: int, K: int, device="cuda") -> "Workspace":
         return Workspace(load_library().dflash2_verify_workspace_bytes(B, K), device)
 
@@ -204,7 +198,7 @@ def ctx_gate(h: torch.Tensor, Wg: torch.Tensor, out=None):
     return gate
 
 
-def pair_score_walk(cand_idx, cand_U, last_tok, A, Bt, gate, params=None, u_walk=None, ws=None, out=None):
+def pair_score_walk(cand_idx, cand_U, last_tok, A, Bt, gate, params=None, u_walk=None, out=None):
     """dflash2_pair_score_walk.  cand_idx/cand_U [B, K, 16], gate [B, K, D], A/Bt [V, D].
 
     Returns (path_tok [B,K], path_slot [B,K], q_sel [B,K,16], scores [B,K,16,16]).
@@ -214,8 +208,6 @@ def pair_score_walk(cand_idx, cand_U, last_tok, A, Bt, gate, params=None, u_walk
     B, K = cand_idx.shape[0], cand_idx.shape[1]
     V, D = A.shape
     dev = cand_idx.device
-    if ws is None:
-        ws = Workspace.for_walk(B, dev)
     if out is None:
         out = (torch.empty(B, K, dtype=torch.int32, device=dev), torch.empty(B, K, dtype=torch.int32, device=dev),
                torch.empty(B, K, NC, dtype=torch.float32, device=dev),
@@ -225,8 +217,7 @@ def pair_score_walk(cand_idx, cand_U, last_tok, A, Bt, gate, params=None, u_walk
     _check("dflash2_pair_score_walk",
            L.dflash2_pair_score_walk(B, K, _ptr(cand_idx), _ptr(cand_U), _ptr(last_tok), _ptr(A), _ptr(Bt),
                                      _dtype(A), V, D, _ptr(gate), _ptr(p), _ptr(u_walk), _ptr(path_tok),
-                                     _ptr(path_slot), _ptr(q_sel), _ptr(scores), ws.ptr(), ws.nbytes,
-                                     _stream(dev)))
+                                     _ptr(path_slot), _ptr(q_sel), _ptr(scores), _stream(dev)))
     return path_tok, path_slot, q_sel, scores
 
 

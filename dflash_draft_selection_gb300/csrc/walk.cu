@@ -42,7 +42,6 @@ struct WalkArgs {
     int32_t *path_slot;
     float *q_sel;
     float *scores;
-    int32_t *tickets;
 };
 
 // Walk tables of one position's tile, for every predecessor row i: the row
@@ -354,8 +353,29 @@ static size_t walk_smem(int D, int K) {
            static_cast<size_t>(K) * (NC * NC * sizeof(float) + 3 * NC * sizeof(int32_t));
 }
 
+// Whether a cluster of K CTAs with the walk's shared memory at D fits on this
+// GPU at all (cudaOccupancyMaxActiveClusters > 0).  Clusters above the
+// portable 8 must fit in one GPC, so a large K at a large D might not.
+// Cached per device and (K, D).
+static bool walk_cluster_fits(const void *fn, const cudaLaunchConfig_t &cfg, int K, int D) {
+    static signed char fits[64][DFLASH2_MAX_K + 1][7];  // 0 unknown, 1 fits, -1 does not
+    static std::mutex mu;
+    const int dev = current_device();
+    int di = 0;
+    while ((16 << di) < D) ++di;  // D = 16 << di, di in 0..6
+    std::lock_guard<std::mutex> lock(mu);
+    signed char *f = (dev >= 0 && dev < 64) ? &fits[dev][K][di] : nullptr;
+    if (f && *f) return *f > 0;
+    int n = 0;
+    const bool ok = cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0;
+    if (!ok) cudaGetLastError();  // a refused query is an answer here, not a sticky launch error
+    if (f) *f = ok ? 1 : -1;
+    return ok;
+}
+
 // Launch one cluster of K CTAs per request (K up to 15: clusters above the
-// portable 8 are allowed on this GPU once the kernel opts in).
+// portable 8 are allowed on this GPU once the kernel opts in).  UNSUPPORTED
+// when such a cluster cannot be resident at this D.
 template <bool BF16>
 static dflash2_status launch_walk(const WalkArgs &a, cudaStream_t s) {
     const void *fn = reinterpret_cast<const void *>(&k_pair_score_walk<BF16>);
@@ -382,6 +402,8 @@ static dflash2_status launch_walk(const WalkArgs &a, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     attr[1] = pdl_attribute();
     cfg.attrs = attr;
+    cfg.numAttrs = 1;  // the occupancy query takes the cluster shape only
+    if (!walk_cluster_fits(fn, cfg, a.K, a.D)) return DFLASH2_ERR_UNSUPPORTED;
     cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, k_pair_score_walk<BF16>, a) != cudaSuccess) return DFLASH2_ERR_CUDA;
     return after_launch();
@@ -391,28 +413,21 @@ static dflash2_status launch_walk(const WalkArgs &a, cudaStream_t s) {
 
 using namespace dfl;
 
-extern "C" size_t dflash2_pair_score_walk_workspace_bytes(int64_t B) {
-    if (B < 0) return 0;
-    return static_cast<size_t>((B * sizeof(int32_t) + 255) / 256 * 256);
-}
-
 extern "C" dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand_idx,
                                                   const float *cand_U, const int32_t *last_tok,
                                                   const void *A, const void *Bt, dflash2_dtype tdt,
                                                   int64_t V, int32_t D, const float *gate,
                                                   const dflash2_sampling *params, const float *u_walk,
                                                   int32_t *path_tok, int32_t *path_slot, float *q_sel,
-                                                  float *scores, void *ws, size_t ws_bytes,
-                                                  dflash2_stream stream) {
+                                                  float *scores, dflash2_stream stream) {
     if (!dtype_ok(tdt) || B < 0 || K < 1 || K > DFLASH2_MAX_K || V < NC || V >= (int64_t(1) << 31) ||
         D < 16 || D > 1024 || (D & (D - 1)) != 0)
         return DFLASH2_ERR_INVALID_ARG;
     if (B == 0) return DFLASH2_OK;
     if (!cand_idx || !cand_U || !last_tok || !A || !Bt || !gate || !path_tok || !path_slot || !q_sel ||
-        !scores || !ws || !aligned16(A) || !aligned16(Bt))
+        !scores || !aligned16(A) || !aligned16(Bt))
         return DFLASH2_ERR_INVALID_ARG;
     if (params && !u_walk) return DFLASH2_ERR_INVALID_ARG;
-    if (ws_bytes < dflash2_pair_score_walk_workspace_bytes(B)) return DFLASH2_ERR_WORKSPACE;
     if (B > 65535) return DFLASH2_ERR_UNSUPPORTED;
     WalkArgs a;
     a.B = B;
@@ -431,7 +446,6 @@ extern "C" dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const in
     a.path_slot = path_slot;
     a.q_sel = q_sel;
     a.scores = scores;
-    a.tickets = static_cast<int32_t *>(ws);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     return tdt == DFLASH2_BF16 ? launch_walk<true>(a, s) : launch_walk<false>(a, s);
 }

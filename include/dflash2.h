@@ -23,8 +23,12 @@
  *     request in `status` (DFLASH2_ST_*) or as -1 / NaN outputs.
  *   - Workspaces (`ws`) are caller-provided device buffers of at least the
  *     size returned by the matching *_workspace_bytes function.  They must be
- *     zero-filled once before first use; every call leaves them zeroed again.
- *     Two calls that share a workspace must not run concurrently.
+ *     zero-filled once before first use; every call that runs to the end
+ *     leaves them zeroed again.  After a call that returned DFLASH2_ERR_CUDA,
+ *     or after dflash2_device_error reported a nonzero code (a kernel gave up
+ *     on a bounded wait), zero-fill the workspaces of the calls involved
+ *     again before reusing them.  Two calls that share a workspace must not
+ *     run concurrently.
  *   - The first call on a device performs one-time set-up (device attributes,
  *     kernel attributes); make it before any stream capture.  Later calls are
  *     capturable into CUDA graphs.
@@ -178,21 +182,21 @@ dflash2_status dflash2_ctx_gate(const void *h, dflash2_dtype dt, int64_t n, int6
  * take the first slot whose cumulative q exceeds u_walk.  A step whose row
  * holds a NaN, or only -inf, ends the walk: that step and the rest get
  * token -1, slot -1 and NaN q.  Ids outside [0, V) give NaN scores.
- * ws: dflash2_pair_score_walk_workspace_bytes(B) bytes (one ticket per
- *   request; the current kernel keeps its per-request state in the shared
- *   memory of the request's thread-block cluster and leaves ws untouched).
+ * No workspace: one thread-block cluster of K CTAs per request keeps the
+ *   request's state in its shared memory.
  * Errors: INVALID_ARG for NULL/misaligned pointers, B < 0, K outside 1..15,
- * D not a power of two in 16..1024, V < 16, u_walk NULL with params set.
+ * D not a power of two in 16..1024, V < 16, u_walk NULL with params set;
+ * UNSUPPORTED for B > 65535, or when a cluster of K CTAs with the shared
+ * memory that D needs cannot be resident on this GPU (clusters above 8 CTAs
+ * must fit in one GPC; the answer is cached per device, K and D).
  */
-size_t dflash2_pair_score_walk_workspace_bytes(int64_t B);
 dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand_idx,
                                        const float *cand_U, const int32_t *last_tok,
                                        const void *A, const void *Bt, dflash2_dtype tdt, int64_t V,
                                        int32_t D, const float *gate,
                                        const dflash2_sampling *params, const float *u_walk,
                                        int32_t *path_tok, int32_t *path_slot, float *q_sel,
-                                       float *scores, void *ws, size_t ws_bytes,
-                                       dflash2_stream stream);
+                                       float *scores, dflash2_stream stream);
 
 /*
  * dflash2_verify -- [F] Sampled verify (accept with min(1, p/q); on a reject

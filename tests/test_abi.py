@@ -45,7 +45,6 @@ def test_workspace_sizes(lib):
     assert lib.dflash2_verify_workspace_bytes(64, 7) >= 64 * 8 * 520
     assert lib.dflash2_verify_workspace_bytes(1, 0) == 0
     assert lib.dflash2_verify_workspace_bytes(1, 16) == 0
-    assert lib.dflash2_pair_score_walk_workspace_bytes(64) >= 256
     assert lib.dflash2_topk16_workspace_bytes(448) >= 448 * 4
     assert lib.dflash2_topk16_workspace_bytes(-1) == 0
 
@@ -64,11 +63,9 @@ def test_argument_checks_fail_before_any_launch(lib):
     # K outside 1..15
     assert lib.dflash2_verify(p, 1, 2, 16, 128, 128, p, p, p, p, None, None, None, 0, p, p, p, p, 1 << 20,
                               None) == bad
-    assert lib.dflash2_pair_score_walk(2, 0, p, p, p, p, p, 1, 128, 256, p, None, None, p, p, p, p, p, 256,
-                                       None) == bad
+    assert lib.dflash2_pair_score_walk(2, 0, p, p, p, p, p, 1, 128, 256, p, None, None, p, p, p, p, None) == bad
     # D not a power of two
-    assert lib.dflash2_pair_score_walk(2, 3, p, p, p, p, p, 1, 128, 100, p, None, None, p, p, p, p, p, 256,
-                                       None) == bad
+    assert lib.dflash2_pair_score_walk(2, 3, p, p, p, p, p, 1, 128, 100, p, None, None, p, p, p, p, None) == bad
     assert lib.dflash2_ctx_gate(p, 1, 4, 128, p, 48, p, None) == bad
     # bf16 hidden not a multiple of 64
     assert lib.dflash2_ctx_gate(p, 1, 4, 100, p, 256, p, None) == bad

@@ -65,6 +65,19 @@ def test_sampled(ref, T):
     run(ref, 16, 7, 5000, 256, seed=3, T=T, scale=1.0)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_largest_cluster_at_the_largest_D(ref, dtype):
+    """K = 15 (a 15-CTA cluster, above the portable 8) at D = 1024 (the most
+    shared memory a CTA of the walk takes): either the cluster can be resident
+    and the result matches the oracle, or the call returns UNSUPPORTED and
+    launches nothing."""
+    try:
+        run(ref, 3, 15, 3000, 1024, seed=15, T=1.0, dtype=dtype)
+    except d2.DFlash2Error as e:
+        assert e.code == 2, e  # DFLASH2_ERR_UNSUPPORTED
+        assert d2.device_error() == 0
+
+
 def test_zero_A_is_top1_chain(ref):
     dev = cuda_or_skip()
     B, K, V, D = 4, 7, 1000, 256
@@ -92,12 +105,11 @@ def test_filtered_candidates_never_drawn(ref):
     last_g = last.repeat(B).to(dev)
     gate_g = gate.view(1, K, D).repeat(B, 1, 1).to(dev)
     params = d2.sampling_params([1.0] * B, [0] * B, [1.0] * B, device=dev)
-    ws = d2.Workspace.for_walk(B, dev)
     gen = torch.Generator(device=dev).manual_seed(6)
     hist0 = torch.zeros(16, dtype=torch.int64, device=dev)
     for _ in range(40):  # 40 * 25000 = 1M walks
         pt, ps, q, S = d2.pair_score_walk(idx_g, U_g, last_g, A.to(dev), Bt.to(dev), gate_g, params=params,
-                                          u_walk=torch.rand(B, K, generator=gen, device=dev), ws=ws)
+                                          u_walk=torch.rand(B, K, generator=gen, device=dev))
         assert not torch.isin(ps[:, 0], torch.tensor([3, 9, 15], device=dev)).any()
         assert not torch.isin(ps[:, 1], torch.tensor([0, 5], device=dev)).any()
         hist0 += torch.bincount(ps[:, 0].long(), minlength=16)
