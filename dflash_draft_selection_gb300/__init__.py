@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     load_library,
     pair_score_walk,
     sampling_params,
+    test_hold,
     topk16,
     topk16_noalloc,
     verify,

@@ -61,8 +61,9 @@ def load_library():
         L.dflash2_status_string.argtypes = [i32]
         L.dflash2_status_string.restype = ctypes.c_char_p
         L.dflash2_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+        L.dflash2_test_hold.argtypes = [vp, i64]
         for fn in ("dflash2_topk16", "dflash2_topk16_noalloc", "dflash2_ctx_gate", "dflash2_pair_score_walk",
-                   "dflash2_verify", "dflash2_conv2tap", "dflash2_device_error"):
+                   "dflash2_verify", "dflash2_conv2tap", "dflash2_device_error", "dflash2_test_hold"):
             getattr(L, fn).restype = i32
         _lib = L
         return _lib
@@ -263,3 +264,11 @@ def device_error(clear: bool = False) -> int:
     code = ctypes.c_uint32(0)
     _check("dflash2_device_error", L.dflash2_device_error(ctypes.byref(code), int(clear)))
     return code.value
+
+
+def test_hold(flag=None, max_cycles: int = 0):
+    """dflash2_test_hold: with `flag` (a CUDA int32 tensor of one element) set, later scan
+    kernels wait on it for at most `max_cycles` before their first copy; None switches it off."""
+    L = load_library()
+    _need_cuda(flag)
+    _check("dflash2_test_hold", L.dflash2_test_hold(_ptr(flag), int(max_cycles) if flag is not None else 0))

@@ -14,7 +14,7 @@ constexpr float NEG_INF = -__builtin_huge_valf();
 constexpr float LOG2E = 1.4426950408889634f;
 
 // Error codes written to a translation unit's error word.
-constexpr uint32_t ERR_WAIT_TIMEOUT = 1u;
+constexpr uint32_t ERR_WAIT_TIMEOUT = DFLASH2_DEVERR_WAIT_TIMEOUT;
 
 // ------------------------------------------------------------------ PTX ----
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {

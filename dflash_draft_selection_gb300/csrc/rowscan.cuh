@@ -74,7 +74,14 @@ struct ScanGeom {
     int64_t total;        // rows * cpr
     const dflash2_sampling *params;
     int64_t rows_per_param;
+    // Test hook (dflash2_test_hold): NULL, or a device word that every
+    // streaming warp waits on, for at most hold_cycles, before its first copy.
+    const unsigned int *hold;
+    long long hold_cycles;
 };
+
+// The hook's current setting, process-wide (host side; set by dflash2_test_hold).
+void scan_hold(const unsigned int **flag, long long *cycles);
 
 // Partial result of a row reduced by several CTAs.
 struct PartRec {
@@ -115,6 +122,7 @@ inline ScanGeom make_geom(const void *logits, int64_t ld, int es, int64_t V, int
     g.total = rows * g.cpr;
     g.params = params;
     g.rows_per_param = rows_per_param;
+    scan_hold(&g.hold, &g.hold_cycles);
     return g;
 }
 
@@ -202,8 +210,23 @@ __device__ __forceinline__ void stream_issue(ScanSmem &sm, const ScanGeom &g, Wa
     }
 }
 
+// Test hook: lane 0 waits until *flag is nonzero, for at most max_cycles SM
+// clock cycles.  True if the word was seen set.
+__device__ __forceinline__ bool hold_wait(const unsigned int *flag, long long max_cycles) {
+    const long long t0 = clock64();
+    while (*reinterpret_cast<const volatile unsigned int *>(flag) == 0) {
+        if (clock64() - t0 > max_cycles) return false;
+        __nanosleep(256);
+    }
+    return true;
+}
+
+// Set up warp w's chunk stream over flat chunks [begin, end) and issue its
+// first copies.  With the test hook set the warp first waits for the hook's
+// word; if the wait runs out, the warp issues nothing, flags the error word
+// and goes through its rows as after any time-out (every row bad).
 __device__ __forceinline__ void stream_start(ScanSmem &sm, const ScanGeom &g, WarpStream &ws, int64_t begin,
-                                             int64_t end, int w, int lane) {
+                                             int64_t end, int w, int lane, unsigned int *err_word) {
     const int64_t len = end - begin;
     ws.n_w = len > w ? static_cast<int>((len - w + SCAN_WARPS - 1) / SCAN_WARPS) : 0;
     const int64_t f0 = begin + w;
@@ -215,7 +238,15 @@ __device__ __forceinline__ void stream_start(ScanSmem &sm, const ScanGeom &g, Wa
     ws.head = 0;
     ws.pol = l2_policy_evict_first();
     ws.aborted = false;
-    for (int i = 0; i < WSTAGES && ws.iss_k < ws.n_w; ++i) stream_issue(sm, g, ws, w, lane);
+    if (g.hold != nullptr) {
+        int seen = 1;
+        if (lane == 0) seen = hold_wait(g.hold, g.hold_cycles) ? 1 : 0;
+        if (!__shfl_sync(FULL, seen, 0)) {
+            ws.aborted = true;
+            if (lane == 0) atomicOr(err_word, ERR_WAIT_TIMEOUT);
+        }
+    }
+    for (int i = 0; i < WSTAGES && !ws.aborted && ws.iss_k < ws.n_w; ++i) stream_issue(sm, g, ws, w, lane);
 }
 
 // After a time-out: wait a bounded time for the copies still in flight.

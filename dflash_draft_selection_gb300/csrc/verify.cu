@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()
     const int64_t r_first = begin / g.cpr, r_last = (end - 1) / g.cpr;
     if (w < SCAN_WARPS) {
         WarpStream ws;
-        stream_start(sm, g, ws, begin, end, w, lane);
+        stream_start(sm, g, ws, begin, end, w, lane, &g_err_verify);
         for (int64_t row = r_first; row <= r_last; ++row) {
             const int rrel = static_cast<int>(row - r_first);
             int w0;

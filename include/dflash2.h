@@ -256,9 +256,27 @@ const char *dflash2_status_string(dflash2_status s);
 /*
  * Error word of the library's kernels on the current device: nonzero after a
  * kernel gave up on a bounded wait (it then wrote -1 / NaN outputs instead of
- * hanging).  Synchronises the device.  clear != 0 resets the word.
+ * hanging; the word then holds DFLASH2_DEVERR_WAIT_TIMEOUT).  Synchronises
+ * the device.  clear != 0 resets the word.
  */
+#define DFLASH2_DEVERR_WAIT_TIMEOUT 1u
 dflash2_status dflash2_device_error(uint32_t *code, int clear);
+
+/*
+ * dflash2_test_hold -- no counterpart on the pages: a test hook of this
+ * library, for exercising the bounded waits without a GPU fault.  With `flag`
+ * set (a 4-byte aligned device word), every streaming warp of every
+ * dflash2_topk16 / dflash2_topk16_noalloc / dflash2_verify kernel launched
+ * afterwards by this process first waits until *flag is nonzero, giving up
+ * after max_cycles SM clock cycles (1 .. 2^32).  A warp that gives up issues
+ * no copy, sets the device error word (DFLASH2_DEVERR_WAIT_TIMEOUT) and goes
+ * through its rows as after any time-out: their outputs are -1 / NaN, and a
+ * verify request that reads such a row gets status DFLASH2_ST_NAN.  flag NULL
+ * switches the hook off.  Kernels already launched or captured keep the
+ * setting they were launched with.
+ * Errors: INVALID_ARG for a misaligned flag or max_cycles out of range.
+ */
+dflash2_status dflash2_test_hold(const uint32_t *flag, int64_t max_cycles);
 
 #ifdef __cplusplus
 }
