@@ -305,37 +305,21 @@ def run_ours(args, rank, world, local):
     value = whole_job_rate(shp.B, world, args.steps, ms / 1e3)
 
     # ---- per-kernel durations: eager steps queued behind a sleep kernel ----
-    kern = {}
-    if not args.no_kernel_pass:
-        n = min(args.steps, 400)
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n)]
-        torch.cuda._sleep(int(1e6 * n))  # ~0.5 ms of GPU time per step: the CPU enqueues ahead of the GPU
-        for i in range(n):
-            inp = chain.sets[i % len(chain.sets)]
-            evs[i][0].record(stream)
-            for j, k in enumerate(Chain.ORDER):
-                chain.call(k, inp)
-                evs[i][j + 1].record(stream)
-        torch.cuda.synchronize()
-        for j, k in enumerate(Chain.ORDER):
-            kern[k] = sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n)) / n
+    kern = {} if args.no_kernel_pass else kernel_pass(chain, stream, min(args.steps, 400))
     algo = algorithmic_bytes(shp)
     peak, peak_kind = measured_peaks()
     roof = None
     if kern:
-        dom = max(("k_topk16", "k_verify"), key=lambda k: kern[k])
-        achieved = algo[dom] / (kern[dom] * 1e-3) / 1e9
-        traffic = profiled_traffic(dom, args.config)
-        roof = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": peak_kind,
-                "algorithmic_bytes": algo[dom], "avg_launch_us": round(kern[dom] * 1e3, 2),
-                "kernels_us": {k: round(v * 1e3, 2) for k, v in kern.items()},
-                "step_bytes_frac_of_peak": round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9 / peak, 4)}
+        roof = roofline(kern, algo, ms_per_step, peak, peak_kind, args.config)
 
-    # ---- the drafter-side conv (not part of the 4-call step): its own HBM roofline ----
+    # ---- the other workloads (sampled; stress) and the drafter-side conv, each with its own roofline ----
     aux = None
     if not args.no_kernel_pass:
-        aux = {"conv2tap": time_conv(dev, peak)}
+        aux = {}
+        for name in AUX_WORKLOADS:
+            if name != args.config:
+                aux[name] = time_workload(name, dev, peak, peak_kind)
+        aux["conv2tap"] = time_conv(dev, peak)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -364,6 +348,77 @@ def run_ours(args, rank, world, local):
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+AUX_WORKLOADS = ("27b_greedy", "27b_sampled", "stress")
+
+
+def kernel_pass(chain, stream, n):
+    """Mean duration of each kernel of the step over n eager steps, queued behind a sleep kernel so that
+    the CPU enqueues ahead of the GPU; CUDA events on the launching stream between the calls."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(Chain.ORDER) + 1)] for _ in range(n)]
+    torch.cuda._sleep(int(1e6 * n))
+    for i in range(n):
+        inp = chain.sets[i % len(chain.sets)]
+        evs[i][0].record(stream)
+        for j, k in enumerate(Chain.ORDER):
+            chain.call(k, inp)
+            evs[i][j + 1].record(stream)
+    torch.cuda.synchronize()
+    return {k: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n)) / n for j, k in enumerate(Chain.ORDER)}
+
+
+def roofline(kern, algo, ms_per_step, peak, peak_kind, workload):
+    """The dominant scan's HBM roofline (algorithmic bytes / its mean launch time) and the whole step's."""
+    dom = max(("k_topk16", "k_verify"), key=lambda k: kern[k])
+    achieved = algo[dom] / (kern[dom] * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(dom, workload), "peak_source": peak_kind,
+            "algorithmic_bytes": algo[dom], "avg_launch_us": round(kern[dom] * 1e3, 2),
+            "kernels_us": {k: round(v * 1e3, 2) for k, v in kern.items()},
+            "step_bytes_frac_of_peak": round(sum(algo.values()) / (ms_per_step * 1e-3) / 1e9 / peak, 4)}
+
+
+def time_workload(name, dev, peak, peak_kind, steps=30):
+    """Another workload's step: graphs of 3 consecutive steps (3 rotating input sets, every set larger
+    than L2) timed with CUDA events, then the per-kernel pass."""
+    import torch
+
+    from dflash_draft_selection_gb300 import synth
+    shp = synth.WORKLOADS[name]
+    chain = Chain(shp, dev)
+    nsets = len(chain.sets)
+    cap = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(cap):
+        for i in range(max(3, nsets)):
+            chain.step(i)
+        cap.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(nsets):
+                chain.step(i)
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // nsets)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_per_step = e0.elapsed_time(e1) / (reps * nsets)
+    kern = kernel_pass(chain, stream, min(steps, 60))
+    algo = algorithmic_bytes(shp)
+    out = {"workload": name, "B": shp.B, "K": shp.K, "V": shp.V,
+           "sampling": "greedy" if shp.temperature == 0 else
+           f"T={shp.temperature},top_k={shp.top_k},top_p={shp.top_p}",
+           "value": round(shp.B / (ms_per_step * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms_per_step, 5),
+           "steps": reps * nsets, "roofline": roofline(kern, algo, ms_per_step, peak, peak_kind, name)}
+    del chain, g
+    torch.cuda.empty_cache()
+    return out
 
 
 def time_conv(dev, peak, reps=50):
