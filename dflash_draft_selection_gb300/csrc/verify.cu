@@ -12,7 +12,12 @@
 // One launch: persistent CTAs scan the B*(K+1) target rows (argmax for greedy
 // requests, the filtered top-k distribution p for sampled ones) and publish a
 // small record per row in the workspace; a per-request ticket lets the CTA
-// that completes a request's last row run that request's accept walk.
+// that completes a request's last row run that request's accept walk.  For a
+// sampled request each row's record also carries that position's decisions
+// -- the checks of its q row, whether its drafted token is accepted, and the
+// token a reject there (or, for the bonus row, the bonus) would emit -- taken
+// when the row is finished, so that the accept walk reads them all at once
+// and only picks the first reject.
 #include "filter.cuh"
 #include "host.hpp"
 #include "rowscan.cuh"
@@ -24,6 +29,12 @@ static __device__ unsigned int g_err_verify;
 struct TRec {
     int32_t n;       // support size of p (1 for greedy rows)
     int32_t flags;   // DFLASH2_ST_* of the row
+    // Sampled rows with flags == 0 (see row_decide): position t < K: qflag
+    // (DFLASH2_ST_* of its q row and slot), accepted, and emit (the residual
+    // draw when not accepted); the bonus row K: emit (the bonus draw).
+    int32_t qflag;
+    int32_t accepted;
+    int32_t emit;
     int32_t ids[DFLASH2_MAX_TOPK];
     float p[DFLASH2_MAX_TOPK];
 };
@@ -47,9 +58,16 @@ struct VerifyArgs {
 constexpr size_t TICKET_BYTES_ALIGN = 256;
 
 // ---------------------------------------------------------------- records --
+// The row's record.  For a sampled row also returns p's support as the
+// accept walk reads it: entry i = r*32 + lane in (id[r], p[r]), -1 / 0 past
+// the kept count *rn.  Returns the row's flags.
 template <int R>
-__device__ __forceinline__ void finalize_target(const RowResult<R> &res, const RowTask &task, TRec *rec, int lane) {
+__device__ __forceinline__ int32_t finalize_target(const RowResult<R> &res, const RowTask &task, TRec *rec, int lane,
+                                                   int32_t (&id)[2], float (&pr)[2], int *rn) {
     int32_t flags = DFLASH2_ST_OK;
+    id[0] = id[1] = -1;
+    pr[0] = pr[1] = 0.0f;
+    *rn = 0;
     if (task.mode == MODE_ARGMAX) {
         const bool bad = res.bad || res.best == 0 || !isfinite(key_val(res.best));
         if (bad) flags = DFLASH2_ST_NAN;
@@ -72,14 +90,18 @@ __device__ __forceinline__ void finalize_target(const RowResult<R> &res, const R
             for (int r = 0; r < R; ++r) {
                 const int p = r * 32 + lane;
                 if (p < kept) {
-                    rec->ids[p] = key_idx(res.list.k[r]);
-                    rec->p[p] = e[r] * inv;
+                    id[r] = key_idx(res.list.k[r]);
+                    pr[r] = e[r] * inv;
+                    rec->ids[p] = id[r];
+                    rec->p[p] = pr[r];
                 }
             }
+            *rn = kept;
             if (lane == 0) rec->n = kept;
         }
     }
     if (lane == 0) rec->flags = flags;
+    return flags;
 }
 
 // ------------------------------------------------------------ accept walk --
@@ -144,6 +166,66 @@ __device__ int32_t draw_ascending(const int32_t (&id)[2], const float (&w)[2], i
 __device__ __forceinline__ int32_t ldcg_i(const int32_t *p) { return __ldcg(p); }
 __device__ __forceinline__ float ldcg_f(const float *p) { return __ldcg(p); }
 
+// A sampled request's decisions at target row t of request b (rec), taken
+// when the row is finished; (id, p, rn) is the row's p as finalize_target
+// returns it.  Position t < K: the checks of its q row and slot (qflag: the
+// first failing check, NaN or a negative q before a wrong total before a bad
+// slot), whether u_acc * q < p at the drafted token, and -- when not -- the
+// draw from max(0, p - q) (from p when that has no mass) with u_res[t].  The
+// bonus row t = K: the draw from p with u_res[K].  The accept walk uses the
+// decisions of the rows up to its first reject only.  Warp-uniform.
+__device__ void row_decide(const VerifyArgs &a, int64_t b, int t, const int32_t (&id)[2], const float (&p)[2],
+                           int rn, TRec *rec, DrawScratch &sc, int lane) {
+    const int K = a.K;
+    int32_t qflag = DFLASH2_ST_OK, accepted = 0, emit = -1;
+    if (t < K) {
+        const int64_t o = (b * K + t) * NC;
+        const float qv = lane < NC ? a.q_sel[o + lane] : 0.0f;
+        const int js = a.path_slot[b * K + t];
+        const int32_t d = a.path_tok[b * K + t];
+        if (__any_sync(FULL, lane < NC && (!isfinite(qv) || qv < 0.0f))) {
+            qflag = DFLASH2_ST_NAN;
+        } else {
+            const float s = warp_sum(qv);
+            if (!(a.flags & DFLASH2_VERIFY_TRUST_Q) && fabsf(s - 1.0f) > 1e-3f)
+                qflag = DFLASH2_ST_BAD_Q;
+            else if (js < 0 || js >= NC || a.cand_idx[o + js] != d)
+                qflag = DFLASH2_ST_BAD_Q;
+        }
+        if (qflag == DFLASH2_ST_OK) {
+            const float pd = warp_sum((id[0] == d && d >= 0 ? p[0] : 0.0f) + (id[1] == d && d >= 0 ? p[1] : 0.0f));
+            const float qd = a.q_sel[o + js];
+            accepted = a.u_acc[b * K + t] * qd < pd ? 1 : 0;
+            if (!accepted) {
+                // residual max(0, p - q) over the support of p
+                const int32_t cc = lane < NC ? a.cand_idx[o + lane] : -1;
+                float r_[2] = {0.0f, 0.0f};
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float qj_of = 0.0f;
+                    for (int j = 0; j < NC; ++j) {
+                        const int32_t cj = __shfl_sync(FULL, cc, j);
+                        const float qj = __shfl_sync(FULL, qv, j);
+                        if (cj == id[r]) qj_of = qj;
+                    }
+                    const float diff = p[r] - qj_of;
+                    r_[r] = (r * 32 + lane < rn && diff > 0.0f) ? diff : 0.0f;
+                }
+                const float Z = warp_sum(r_[0] + r_[1]);
+                const float u = a.u_res[b * (K + 1) + t];
+                emit = Z > 1e-12f ? draw_ascending(id, r_, rn, u, sc, lane) : draw_ascending(id, p, rn, u, sc, lane);
+            }
+        }
+    } else {
+        emit = draw_ascending(id, p, rn, a.u_res[b * (K + 1) + K], sc, lane);
+    }
+    if (lane == 0) {
+        rec->qflag = qflag;
+        rec->accepted = accepted;
+        rec->emit = emit;
+    }
+}
+
 // The accept walk of request b (consumer warp 0 of the CTA that completed the
 // request's rows).
 template <bool SAMPLED>
@@ -175,97 +257,21 @@ __device__ void accept_request(const VerifyArgs &a, const dflash2_sampling *para
         }
         return;
     }
-    if (st == DFLASH2_ST_OK && !greedy) {
-        for (int t = 0; t < K; ++t) {
-            const int64_t o = (b * K + t) * NC;
-            const float qv = lane < NC ? a.q_sel[o + lane] : 0.0f;
-            if (__any_sync(FULL, lane < NC && (!isfinite(qv) || qv < 0.0f))) {
-                st = DFLASH2_ST_NAN;
-                break;
-            }
-            const float s = warp_sum(qv);
-            if (!(a.flags & DFLASH2_VERIFY_TRUST_Q) && fabsf(s - 1.0f) > 1e-3f) {
-                st = DFLASH2_ST_BAD_Q;
-                break;
-            }
-            const int js = a.path_slot[b * K + t];
-            if (js < 0 || js >= NC || a.cand_idx[o + js] != a.path_tok[b * K + t]) {
-                st = DFLASH2_ST_BAD_Q;
-                break;
-            }
-        }
-    }
     int n = 0;
     int32_t emit = -1;
     if (st == DFLASH2_ST_OK) {
-        bool stopped = false;
-        for (int t = 0; t < K && !stopped; ++t) {
-            const int32_t d = a.path_tok[b * K + t];
-            if (greedy) {
-                const int32_t g = ldcg_i(&rec[t].ids[0]);
-                if (d == g) {
-                    ++n;
-                } else {
-                    emit = g;
-                    stopped = true;
-                }
-                continue;
-            }
-            const int rn = ldcg_i(&rec[t].n);
-            int32_t id[2];
-            float p[2];
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int i = r * 32 + lane;
-                id[r] = i < rn ? ldcg_i(&rec[t].ids[i]) : -1;
-                p[r] = i < rn ? ldcg_f(&rec[t].p[i]) : 0.0f;
-            }
-            const float pd = warp_sum((id[0] == d && d >= 0 ? p[0] : 0.0f) +
-                                      (id[1] == d && d >= 0 ? p[1] : 0.0f));
-            const int64_t o = (b * K + t) * NC;
-            const float qd = a.q_sel[o + a.path_slot[b * K + t]];
-            if (a.u_acc[b * K + t] * qd < pd) {
-                ++n;
-                continue;
-            }
-            // residual max(0, p - q) over the support of p
-            const float qc = lane < NC ? a.q_sel[o + lane] : 0.0f;
-            const int32_t cc = lane < NC ? a.cand_idx[o + lane] : -1;
-            float r_[2] = {0.0f, 0.0f};
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                float qv = 0.0f;
-                for (int j = 0; j < NC; ++j) {
-                    const int32_t cj = __shfl_sync(FULL, cc, j);
-                    const float qj = __shfl_sync(FULL, qc, j);
-                    if (cj == id[r]) qv = qj;
-                }
-                const float diff = p[r] - qv;
-                r_[r] = (r * 32 + lane < rn && diff > 0.0f) ? diff : 0.0f;
-            }
-            const float Z = warp_sum(r_[0] + r_[1]);
-            const float u = a.u_res[b * (K + 1) + t];
-            if (Z > 1e-12f)
-                emit = draw_ascending(id, r_, rn, u, sc, lane);
-            else
-                emit = draw_ascending(id, p, rn, u, sc, lane);
-            stopped = true;
-        }
-        if (!stopped) {
-            if (greedy) {
-                emit = ldcg_i(&rec[K].ids[0]);
-            } else {
-                const int rn = ldcg_i(&rec[K].n);
-                int32_t id[2];
-                float p[2];
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const int i = r * 32 + lane;
-                    id[r] = i < rn ? ldcg_i(&rec[K].ids[i]) : -1;
-                    p[r] = i < rn ? ldcg_f(&rec[K].p[i]) : 0.0f;
-                }
-                emit = draw_ascending(id, p, rn, a.u_res[b * (K + 1) + K], sc, lane);
-            }
+        // lane t <= K holds row t's decisions (row_decide); the first failing
+        // q check decides the status, else the first reject ends the prefix
+        const int32_t qf = lane < K ? ldcg_i(&rec[lane].qflag) : DFLASH2_ST_OK;
+        const int32_t acc = lane < K ? ldcg_i(&rec[lane].accepted) : 1;
+        const int32_t em = lane <= K ? ldcg_i(&rec[lane].emit) : -1;
+        const uint32_t badq = __ballot_sync(FULL, qf != DFLASH2_ST_OK);
+        if (badq) {
+            st = __shfl_sync(FULL, qf, __ffs(badq) - 1);
+        } else {
+            const uint32_t rej = __ballot_sync(FULL, lane < K && acc == 0);
+            n = rej ? __ffs(rej) - 1 : K;
+            emit = __shfl_sync(FULL, em, n);
         }
     }
     for (int i = lane; i <= K; i += 32) {
@@ -362,7 +368,12 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()
             continue;
         }
         if (done) {
-            finalize_target<R>(res, task, rec, lane);
+            int32_t id[2];
+            float pr[2];
+            int rn;
+            const int32_t fl = finalize_target<R>(res, task, rec, lane, id, pr, &rn);
+            if (SAMPLED && task.mode == MODE_TOPN && fl == DFLASH2_ST_OK)
+                row_decide(a, row / (a.K + 1), static_cast<int>(row % (a.K + 1)), id, pr, rn, rec, sc, lane);
             row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
         }
     }
