@@ -107,7 +107,6 @@ __device__ __forceinline__ int32_t finalize_target(const RowResult<R> &res, cons
 // ------------------------------------------------------------ accept walk --
 struct DrawScratch {
     int32_t ids[DFLASH2_MAX_TOPK];
-    float w[DFLASH2_MAX_TOPK];
     int32_t sid[DFLASH2_MAX_TOPK];
     float sw[DFLASH2_MAX_TOPK];
 };
@@ -116,16 +115,15 @@ static_assert(sizeof(DrawScratch) <= sizeof(ScanSmem::scratch), "the draw scratc
 // Inverse CDF over the entries sorted by ascending token id: the first entry
 // whose running weight exceeds u * (total weight); if rounding leaves none,
 // the last entry with a positive weight.  Entries i < n are (id_i, w_i) with
-// i = r*32 + lane; ids are distinct.  Warp-uniform; returns the token.
+// i = r*32 + lane; ids are distinct.  The entries are ranked by id in shared
+// memory; then lane l holds sorted entries l and l + 32, and the running
+// weights come from two warp scans.  Warp-uniform; returns the token.
 __device__ int32_t draw_ascending(const int32_t (&id)[2], const float (&w)[2], int n, float u,
                                   DrawScratch &sc, int lane) {
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
         const int i = r * 32 + lane;
-        if (i < n) {
-            sc.ids[i] = id[r];
-            sc.w[i] = w[r];
-        }
+        if (i < n) sc.ids[i] = id[r];
     }
     __syncwarp();
     int rank[2] = {0, 0};
@@ -143,24 +141,27 @@ __device__ int32_t draw_ascending(const int32_t (&id)[2], const float (&w)[2], i
         }
     }
     __syncwarp();
-    int32_t pick = -1;
-    if (lane == 0) {
-        float Z = 0.0f;
-        for (int i = 0; i < n; ++i) Z += sc.sw[i];
-        const float thr = u * Z;
-        float cum = 0.0f;
-        int32_t last = -1;
-        for (int i = 0; i < n; ++i) {
-            const float wi = sc.sw[i];
-            if (wi <= 0.0f) continue;
-            cum += wi;
-            last = sc.sid[i];
-            if (pick < 0 && cum > thr) pick = sc.sid[i];
-        }
-        if (pick < 0) pick = last;
-    }
+    const float w0 = lane < n ? sc.sw[lane] : 0.0f;
+    const float w1 = lane + 32 < n ? sc.sw[lane + 32] : 0.0f;
+    const float p0 = w0 > 0.0f ? w0 : 0.0f, p1 = w1 > 0.0f ? w1 : 0.0f;
+    const float thr = u * warp_sum(p0 + p1);
+    const float c0 = warp_inclusive_scan(p0, lane);
+    const float c1 = warp_inclusive_scan(p1, lane) + __shfl_sync(FULL, c0, 31);
+    const uint32_t h0 = __ballot_sync(FULL, w0 > 0.0f && c0 > thr);
+    const uint32_t h1 = __ballot_sync(FULL, w1 > 0.0f && c1 > thr);
+    const uint32_t l0 = __ballot_sync(FULL, w0 > 0.0f), l1 = __ballot_sync(FULL, w1 > 0.0f);
+    int pos = -1;
+    if (h0)
+        pos = __ffs(h0) - 1;
+    else if (h1)
+        pos = 32 + __ffs(h1) - 1;
+    else if (l1)
+        pos = 32 + 31 - __clz(l1);
+    else if (l0)
+        pos = 31 - __clz(l0);
+    const int32_t pick = pos >= 0 ? sc.sid[pos] : -1;
     __syncwarp();
-    return __shfl_sync(FULL, pick, 0);
+    return pick;
 }
 
 __device__ __forceinline__ int32_t ldcg_i(const int32_t *p) { return __ldcg(p); }
