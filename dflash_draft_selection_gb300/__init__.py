@@ -16,6 +16,8 @@ from .binding import (  # noqa: F401
     sampling_params,
     test_hold,
     topk16,
+    topk16_merge,
     topk16_noalloc,
+    topk16_shard,
     verify,
 )

@@ -23,6 +23,7 @@ F32, BF16 = 0, 1
 ST_OK, ST_NAN, ST_BAD_Q, ST_BAD_PARAMS, ST_UNSUPPORTED = 0, 1, 2, 3, 4
 VERIFY_TRUST_Q = 1
 NC = 16
+SHARD_LIST = 64
 
 SAMPLING_DTYPE = np.dtype([("temperature", "<f4"), ("top_k", "<i4"), ("top_p", "<f4")])
 
@@ -50,6 +51,8 @@ def load_library():
         L.dflash2_topk16_workspace_bytes.restype = sz
         L.dflash2_topk16.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp, sz, vp]
         L.dflash2_topk16_noalloc.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp]
+        L.dflash2_topk16_shard.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+        L.dflash2_topk16_merge.argtypes = [i32, i64, vp, vp, vp, vp, i64, vp, i64, vp, vp, vp, vp]
         L.dflash2_ctx_gate.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp]
         L.dflash2_pair_score_walk.argtypes = [i64, i32, vp, vp, vp, vp, vp, i32, i64, i32, vp, vp, vp, vp, vp,
                                               vp, vp, vp]
@@ -62,7 +65,8 @@ def load_library():
         L.dflash2_status_string.restype = ctypes.c_char_p
         L.dflash2_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         L.dflash2_test_hold.argtypes = [vp, i64]
-        for fn in ("dflash2_topk16", "dflash2_topk16_noalloc", "dflash2_ctx_gate", "dflash2_pair_score_walk",
+        for fn in ("dflash2_topk16", "dflash2_topk16_noalloc", "dflash2_topk16_shard", "dflash2_topk16_merge",
+                   "dflash2_ctx_gate", "dflash2_pair_score_walk",
                    "dflash2_verify", "dflash2_conv2tap", "dflash2_device_error", "dflash2_test_hold"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -183,6 +187,51 @@ def topk16_noalloc(logits: torch.Tensor, params=None, rows_per_param: int = 1, V
     _check("dflash2_topk16_noalloc",
            L.dflash2_topk16_noalloc(_ptr(logits), _dtype(logits), rows, V, ld, _ptr(p), rows_per_param,
                                     _ptr(cand_idx), _ptr(cand_U), _ptr(lse), _stream(dev)))
+    return cand_idx, cand_U, lse
+
+
+def topk16_shard(logits: torch.Tensor, id_offset: int, V_total: int, params=None, rows_per_param: int = 1,
+                 V: int | None = None, ws=None, out=None):
+    """dflash2_topk16_shard: one vocabulary slice's partial.  logits [rows, ld] hold tokens id_offset.. .
+    Returns (part_idx [rows, 64] i32, part_z [rows, 64] f32, part_m [rows] f32, part_s [rows] f32)."""
+    L = load_library()
+    _need_cuda(logits)
+    assert logits.dim() == 2 and logits.stride(1) == 1
+    rows, ld = logits.shape[0], logits.stride(0)
+    V = logits.shape[1] if V is None else V
+    dev = logits.device
+    if out is None:
+        out = (torch.empty(rows, SHARD_LIST, dtype=torch.int32, device=dev),
+               torch.empty(rows, SHARD_LIST, dtype=torch.float32, device=dev),
+               torch.empty(rows, dtype=torch.float32, device=dev), torch.empty(rows, dtype=torch.float32, device=dev))
+    pi, pz, pm, ps = out
+    if ws is None:
+        ws = Workspace.for_topk16(rows, dev)
+    p = _params_from(params, dev)
+    _check("dflash2_topk16_shard",
+           L.dflash2_topk16_shard(_ptr(logits), _dtype(logits), rows, V, ld, id_offset, V_total, _ptr(p),
+                                  rows_per_param, _ptr(pi), _ptr(pz), _ptr(pm), _ptr(ps), ws.ptr(), ws.nbytes,
+                                  _stream(dev)))
+    return pi, pz, pm, ps
+
+
+def topk16_merge(part_idx, part_z, part_m, part_s, V_total: int, params=None, rows_per_param: int = 1, out=None):
+    """dflash2_topk16_merge: partials stacked [S, rows, 64] / [S, rows].  Returns (cand_idx, cand_U, lse)."""
+    L = load_library()
+    _need_cuda(part_idx, part_z, part_m, part_s)
+    for t in (part_idx, part_z, part_m, part_s):
+        assert t.is_contiguous()
+    S, rows = part_idx.shape[0], part_idx.shape[1]
+    dev = part_idx.device
+    if out is None:
+        out = (torch.empty(rows, NC, dtype=torch.int32, device=dev),
+               torch.empty(rows, NC, dtype=torch.float32, device=dev),
+               torch.empty(rows, dtype=torch.float32, device=dev))
+    cand_idx, cand_U, lse = out
+    p = _params_from(params, dev)
+    _check("dflash2_topk16_merge",
+           L.dflash2_topk16_merge(S, rows, _ptr(part_idx), _ptr(part_z), _ptr(part_m), _ptr(part_s), V_total,
+                                  _ptr(p), rows_per_param, _ptr(cand_idx), _ptr(cand_U), _ptr(lse), _stream(dev)))
     return cand_idx, cand_U, lse
 
 

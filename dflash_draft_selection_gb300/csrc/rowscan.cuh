@@ -74,6 +74,7 @@ struct ScanGeom {
     int64_t total;        // rows * cpr
     const dflash2_sampling *params;
     int64_t rows_per_param;
+    int64_t V_params;  // vocabulary size the sampling parameters refer to (the whole row's, for a shard)
     // Test hook (dflash2_test_hold): NULL, or a device word that every
     // streaming warp waits on, for at most hold_cycles, before its first copy.
     const unsigned int *hold;
@@ -122,6 +123,7 @@ inline ScanGeom make_geom(const void *logits, int64_t ld, int es, int64_t V, int
     g.total = rows * g.cpr;
     g.params = params;
     g.rows_per_param = rows_per_param;
+    g.V_params = V;
     scan_hold(&g.hold, &g.hold_cycles);
     return g;
 }

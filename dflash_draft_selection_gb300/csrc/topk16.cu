@@ -53,6 +53,90 @@ __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const Ro
     if (lane == 0) lse[row] = L;
 }
 
+// Outputs of a vocabulary shard's partial (dflash2_topk16_shard); part_idx
+// NULL for the ordinary call.
+struct ShardOut {
+    int32_t *part_idx;  // [rows, DFLASH2_SHARD_LIST] global ids, -1 past the row's list
+    float *part_z;      // [rows, DFLASH2_SHARD_LIST] logits, -inf past the list
+    float *part_m;      // [rows] the shard's largest logit
+    float *part_s;      // [rows] sum of exp((z - m) / T') over the shard (0 for filtered rows)
+    int64_t id_offset;  // global id of the shard's token 0
+};
+
+// A shard row's partial: its list's first nsel keys as (global id, logit),
+// the largest logit and the sum of the log normaliser; a row with a NaN or
+// +Inf, bad or unsupported parameters gets -1 ids, m and s NaN.  A slice of
+// masked tokens (every logit -inf) keeps its list, with m = -inf and s = 0.
+// Warp-uniform.
+template <int R>
+__device__ __forceinline__ void finalize_shard(const RowResult<R> &res, const RowTask &task, int64_t row,
+                                               const ShardOut &so, int lane) {
+    const float top = __shfl_sync(FULL, key_val(res.list.k[0]), 0);
+    const float m = task.mode == MODE_TOPN_LSE ? res.m : top;
+    const bool bad = res.bad || task.mode == MODE_SKIP || task.mode == MODE_ARGMAX || m != m || m == INFINITY;
+#pragma unroll
+    for (int r = 0; r < DFLASH2_SHARD_LIST / 32; ++r) {
+        const int p = r * 32 + lane;
+        uint64_t k = 0;
+#pragma unroll
+        for (int rr = 0; rr < R; ++rr)
+            if (rr == r) k = res.list.k[rr];
+        const bool has = !bad && p < task.nsel && k != 0;
+        so.part_idx[row * DFLASH2_SHARD_LIST + p] = has ? static_cast<int32_t>(key_idx(k) + so.id_offset) : -1;
+        so.part_z[row * DFLASH2_SHARD_LIST + p] = has ? key_val(k) : NEG_INF;
+    }
+    if (lane == 0) {
+        so.part_m[row] = bad ? NAN : m;
+        so.part_s[row] = bad ? NAN : (task.mode == MODE_TOPN_LSE && m != NEG_INF ? res.s : 0.0f);
+    }
+}
+
+// Merge of S shard partials, one warp per row: the union of the lists as
+// one list of keys (value, global id), the log normalisers combined, then
+// the same outputs as the whole row's dflash2_topk16.
+__global__ void __launch_bounds__(256) k_topk16_merge(int S, int64_t rows, const int32_t *part_idx,
+                                                      const float *part_z, const float *part_m,
+                                                      const float *part_s, int64_t V_total,
+                                                      const dflash2_sampling *params, int64_t rows_per_param,
+                                                      int32_t *cand_idx, float *cand_U, float *lse) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_trigger();
+    if (row >= rows) return;
+    const RowTask task = decode_row(params, row / rows_per_param, V_total, false);
+    RowResult<2> res;
+    res.list.clear();
+    res.best = 0;
+    res.m = NEG_INF;
+    res.s = 0.0f;
+    res.bad = task.mode == MODE_SKIP;
+    const float c = LOG2E / task.T;
+    for (int sh = 0; sh < S; ++sh) {
+        const int64_t base = (static_cast<int64_t>(sh) * rows + row) * DFLASH2_SHARD_LIST;
+        WarpList<2> o;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int32_t id = part_idx[base + r * 32 + lane];
+            o.k[r] = id >= 0 ? make_key(part_z[base + r * 32 + lane], static_cast<uint32_t>(id)) : 0ull;
+        }
+        res.list.merge(o, lane);  // each partial's list is already in key order
+        const float m2 = part_m[static_cast<int64_t>(sh) * rows + row];
+        const float s2 = part_s[static_cast<int64_t>(sh) * rows + row];
+        if (m2 != m2) res.bad = true;
+        else lse_combine(res.m, res.s, m2, s2, c);
+    }
+    if (task.mode == MODE_SKIP || task.mode == MODE_ARGMAX) {
+        if (lane < NC) {
+            cand_idx[row * NC + lane] = -1;
+            cand_U[row * NC + lane] = NAN;
+        }
+        if (lane == 0) lse[row] = NAN;
+        return;
+    }
+    finalize_draft<2>(res, task, row, cand_idx, cand_U, lse, lane);
+}
+
 // SAMPLED: some request may sample (params given): lists of 64 keys and every
 // row mode; otherwise every row is greedy (top-16 and the log normaliser).
 // Warps 0..SCAN_WARPS-1 stream the CTA's rows; the last warp completes each
@@ -61,7 +145,8 @@ __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const Ro
 template <bool SAMPLED, bool BF16>
 __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_topk16(ScanGeom g, ScanWs sw,
                                                                                   int32_t *cand_idx,
-                                                                                  float *cand_U, float *lse) {
+                                                                                  float *cand_U, float *lse,
+                                                                                  ShardOut so) {
     constexpr int R = SAMPLED ? 2 : 1;
     extern __shared__ unsigned char smem_raw[];
     ScanSmem &sm = *reinterpret_cast<ScanSmem *>(
@@ -83,7 +168,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
             const int rrel = static_cast<int>(row - r_first);
             int w0;
             const int expect = row_warps(g, row, begin, end, &w0);
-            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, false);
+            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V_params, false);
             if (!SAMPLED || task.mode == MODE_TOPN_LSE)
                 scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_topk);
             else if (task.mode == MODE_TOPN)
@@ -98,7 +183,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
     uint32_t tail[SCAN_WARPS] = {0, 0, 0, 0};  // ring keys taken, per streaming warp
     for (int64_t row = r_first; row <= r_last; ++row) {
         const int rrel = static_cast<int>(row - r_first);
-        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, false);
+        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V_params, false);
         const float c = LOG2E / task.T;
         RowResult<R> res;
         bool done;
@@ -111,24 +196,31 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
         } else {
             take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
             if (blockIdx.x == range_owner(g, row * g.cpr)) {
-                if (lane < NC) {
-                    cand_idx[row * NC + lane] = -1;
-                    cand_U[row * NC + lane] = NAN;
+                if (so.part_idx) {
+                    finalize_shard<R>(res, task, row, so, lane);
+                } else {
+                    if (lane < NC) {
+                        cand_idx[row * NC + lane] = -1;
+                        cand_U[row * NC + lane] = NAN;
+                    }
+                    if (lane == 0) lse[row] = NAN;
                 }
-                if (lane == 0) lse[row] = NAN;
             }
             continue;
         }
         if (done) {
             if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
-            finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
+            if (so.part_idx)
+                finalize_shard<R>(res, task, row, so, lane);
+            else
+                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
         }
     }
 }
 
 template <bool SAMPLED, bool BF16>
 static dflash2_status launch_topk16(const ScanGeom &g, const ScanWs &sw, int32_t *cand_idx, float *cand_U,
-                                    float *lse, cudaStream_t stream) {
+                                    float *lse, const ShardOut &so, cudaStream_t stream) {
     const size_t smem = scan_smem_bytes();
     const void *fn = reinterpret_cast<const void *>(&k_topk16<SAMPLED, BF16>);
     const int64_t grid = scan_grid(blocks_per_sm(fn, SCAN_THREADS, smem), sm_count(), g.rows, g.total);
@@ -140,7 +232,7 @@ static dflash2_status launch_topk16(const ScanGeom &g, const ScanWs &sw, int32_t
     cudaLaunchAttribute attr[1] = {pdl_attribute()};
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_topk16<SAMPLED, BF16>, g, sw, cand_idx, cand_U, lse) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, k_topk16<SAMPLED, BF16>, g, sw, cand_idx, cand_U, lse, so) != cudaSuccess)
         return DFLASH2_ERR_CUDA;
     return after_launch();
 }
@@ -169,26 +261,27 @@ extern "C" size_t dflash2_topk16_workspace_bytes(int64_t rows) {
 static dflash2_status topk16_call(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V, int64_t ld,
                                   const dflash2_sampling *params, int64_t rows_per_param, int32_t *cand_idx,
                                   float *cand_U, float *lse, void *ws, size_t ws_bytes, bool clear_tickets,
-                                  cudaStream_t s) {
+                                  cudaStream_t s, const ShardOut &so = ShardOut{}, int64_t V_params = 0) {
     if (!dtype_ok(dt) || rows < 0 || V < NC || V >= (int64_t(1) << 31) || ld < V || rows_per_param < 1)
         return DFLASH2_ERR_INVALID_ARG;
     const int es = esize(dt);
     if ((ld * es) % 16 != 0) return DFLASH2_ERR_INVALID_ARG;
     if (rows == 0) return DFLASH2_OK;
-    if (!logits || !cand_idx || !cand_U || !lse || !ws || !aligned16(logits) || !aligned16(cand_idx) ||
-        !aligned16(cand_U) || !aligned16(lse) || !aligned16(ws) ||
-        (params && (reinterpret_cast<uintptr_t>(params) & 3)))
+    if (!so.part_idx && (!cand_idx || !cand_U || !lse || !aligned16(cand_idx) || !aligned16(cand_U) || !aligned16(lse)))
+        return DFLASH2_ERR_INVALID_ARG;
+    if (!logits || !ws || !aligned16(logits) || !aligned16(ws) || (params && (reinterpret_cast<uintptr_t>(params) & 3)))
         return DFLASH2_ERR_INVALID_ARG;
     if (ws_bytes < scan_ws_bytes(rows)) return DFLASH2_ERR_WORKSPACE;
-    const ScanGeom g = make_geom(logits, ld, es, V, rows, params, rows_per_param);
+    ScanGeom g = make_geom(logits, ld, es, V, rows, params, rows_per_param);
+    if (V_params > 0) g.V_params = V_params;
     const ScanWs sw = scan_ws_at(ws, rows);
     if (clear_tickets && cudaMemsetAsync(sw.tickets, 0, static_cast<size_t>(rows) * sizeof(int32_t), s) != cudaSuccess)
         return DFLASH2_ERR_CUDA;
     if (params == nullptr)
-        return dt == DFLASH2_BF16 ? launch_topk16<false, true>(g, sw, cand_idx, cand_U, lse, s)
-                                  : launch_topk16<false, false>(g, sw, cand_idx, cand_U, lse, s);
-    return dt == DFLASH2_BF16 ? launch_topk16<true, true>(g, sw, cand_idx, cand_U, lse, s)
-                              : launch_topk16<true, false>(g, sw, cand_idx, cand_U, lse, s);
+        return dt == DFLASH2_BF16 ? launch_topk16<false, true>(g, sw, cand_idx, cand_U, lse, so, s)
+                                  : launch_topk16<false, false>(g, sw, cand_idx, cand_U, lse, so, s);
+    return dt == DFLASH2_BF16 ? launch_topk16<true, true>(g, sw, cand_idx, cand_U, lse, so, s)
+                              : launch_topk16<true, false>(g, sw, cand_idx, cand_U, lse, so, s);
 }
 
 extern "C" dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V,
@@ -250,4 +343,53 @@ extern "C" dflash2_status dflash2_topk16_noalloc(const void *logits, dflash2_dty
     // partial records are written before they are read and need no clearing.
     return topk16_call(logits, dt, rows, V, ld, params, rows_per_param, cand_idx, cand_U, lse, ws,
                        dfl::TOPK_NOALLOC_BYTES, true, s);
+}
+
+// ---------------------------------------------------------------------------
+// Vocabulary-sharded top-16: each shard's partial, then the merge.
+extern "C" dflash2_status dflash2_topk16_shard(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V_shard,
+                                               int64_t ld, int64_t id_offset, int64_t V_total,
+                                               const dflash2_sampling *params, int64_t rows_per_param,
+                                               int32_t *part_idx, float *part_z, float *part_m, float *part_s,
+                                               void *ws, size_t ws_bytes, dflash2_stream stream) {
+    if (id_offset < 0 || V_total < V_shard || id_offset + V_shard > V_total || V_total >= (int64_t(1) << 31))
+        return DFLASH2_ERR_INVALID_ARG;
+    if (rows > 0 && (!part_idx || !part_z || !part_m || !part_s || !aligned16(part_idx) || !aligned16(part_z) ||
+                     (reinterpret_cast<uintptr_t>(part_m) & 3) || (reinterpret_cast<uintptr_t>(part_s) & 3)))
+        return DFLASH2_ERR_INVALID_ARG;
+    ShardOut so;
+    so.part_idx = part_idx;
+    so.part_z = part_z;
+    so.part_m = part_m;
+    so.part_s = part_s;
+    so.id_offset = id_offset;
+    if (rows > 0 && !part_idx) return DFLASH2_ERR_INVALID_ARG;
+    return topk16_call(logits, dt, rows, V_shard, ld, params, rows_per_param, nullptr, nullptr, nullptr, ws,
+                       ws_bytes, false, reinterpret_cast<cudaStream_t>(stream), so, V_total);
+}
+
+extern "C" dflash2_status dflash2_topk16_merge(int32_t S, int64_t rows, const int32_t *part_idx, const float *part_z,
+                                               const float *part_m, const float *part_s, int64_t V_total,
+                                               const dflash2_sampling *params, int64_t rows_per_param,
+                                               int32_t *cand_idx, float *cand_U, float *lse, dflash2_stream stream) {
+    if (S < 1 || S > DFLASH2_MAX_SHARDS || rows < 0 || V_total < NC || V_total >= (int64_t(1) << 31) ||
+        rows_per_param < 1)
+        return DFLASH2_ERR_INVALID_ARG;
+    if (rows == 0) return DFLASH2_OK;
+    if (!part_idx || !part_z || !part_m || !part_s || !cand_idx || !cand_U || !lse ||
+        (params && (reinterpret_cast<uintptr_t>(params) & 3)))
+        return DFLASH2_ERR_INVALID_ARG;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffff) return DFLASH2_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_topk16_merge, static_cast<int>(S), rows, part_idx, part_z, part_m, part_s,
+                           V_total, params, rows_per_param, cand_idx, cand_U, lse) != cudaSuccess)
+        return DFLASH2_ERR_CUDA;
+    return after_launch();
 }

@@ -148,6 +148,51 @@ dflash2_status dflash2_topk16_noalloc(const void *logits, dflash2_dtype dt, int6
                                       int32_t *cand_idx, float *cand_U, float *lse, dflash2_stream stream);
 
 /*
+ * Vocabulary-sharded top-16 -- no counterpart on the pages, which run the
+ * drafter with --tp 1 ([F] Known gaps): an addition of this library for an
+ * LM head split over GPUs by vocabulary.  Each GPU reduces its slice of the
+ * vocabulary to a partial (dflash2_topk16_shard); the partials of all slices
+ * are exchanged once (an all-gather of DFLASH2_SHARD_LIST * 8 + 8 bytes per
+ * row and slice, done by the caller); dflash2_topk16_merge then gives the
+ * outputs dflash2_topk16 gives for the whole row, with the same sampling
+ * parameters (top_k and top_p refer to the whole vocabulary V_total).
+ *
+ * dflash2_topk16_shard: logits [rows, ld] of dt hold tokens id_offset ..
+ *   id_offset + V_shard - 1 of each row (V_shard >= 16).  Outputs:
+ *   part_idx [rows, DFLASH2_SHARD_LIST] int32: the slice's best tokens in
+ *     rank order as global ids, as many as the row needs (16; max(16, top_k)
+ *     for a top_k-filtered row), -1 after;
+ *   part_z [rows, DFLASH2_SHARD_LIST] f32: their logits, -inf after;
+ *   part_m [rows] f32: the slice's largest logit;
+ *   part_s [rows] f32: the sum over the slice of exp((z - part_m) / T'), T'
+ *     the temperature (1 for greedy rows); 0 for filtered rows.
+ *   A row with a NaN or +Inf in the slice, or invalid or unsupported
+ *   parameters, gets -1 ids and NaN m and s.  A slice of masked tokens (all
+ *   -inf) is not an error: m = -inf, s = 0.
+ *   ws: dflash2_topk16_workspace_bytes(rows).  Errors: those of dflash2_topk16
+ *   (with V_shard as V), and INVALID_ARG for id_offset < 0 or
+ *   id_offset + V_shard > V_total.
+ *
+ * dflash2_topk16_merge: the partials of the S slices laid out [S, rows, ...]
+ *   (slice s at s * rows * DFLASH2_SHARD_LIST and s * rows); params and
+ *   rows_per_param as for dflash2_topk16.  Outputs cand_idx, cand_U, lse as
+ *   dflash2_topk16's for the whole rows (lse and U equal up to fp32 rounding:
+ *   the log normaliser is summed per slice).  A row with a NaN partial or no
+ *   finite largest logit gets -1 / NaN.  Errors: INVALID_ARG for S outside
+ *   1..DFLASH2_MAX_SHARDS, rows < 0, V_total < 16, NULL pointers.
+ */
+#define DFLASH2_SHARD_LIST 64
+#define DFLASH2_MAX_SHARDS 1024
+dflash2_status dflash2_topk16_shard(const void *logits, dflash2_dtype dt, int64_t rows, int64_t V_shard, int64_t ld,
+                                    int64_t id_offset, int64_t V_total, const dflash2_sampling *params,
+                                    int64_t rows_per_param, int32_t *part_idx, float *part_z, float *part_m,
+                                    float *part_s, void *ws, size_t ws_bytes, dflash2_stream stream);
+dflash2_status dflash2_topk16_merge(int32_t S, int64_t rows, const int32_t *part_idx, const float *part_z,
+                                    const float *part_m, const float *part_s, int64_t V_total,
+                                    const dflash2_sampling *params, int64_t rows_per_param, int32_t *cand_idx,
+                                    float *cand_U, float *lse, dflash2_stream stream);
+
+/*
  * dflash2_ctx_gate -- [P] item 1 "context gate" of the bilinear selector,
  * taken as gate = sigmoid(W_g h) with no bias.
  *

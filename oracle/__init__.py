@@ -44,6 +44,10 @@ def lib():
             L = ctypes.CDLL(_LIB)
             vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
             L.dflash2_ref_topk16.argtypes = [vp, i32, i64, i64, i64, vp, vp, vp, i64, vp, vp, vp, vp]
+            L.dflash2_ref_topk16_shard.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, vp, vp, i64, i32, vp, vp,
+                                                   vp, vp]
+            L.dflash2_ref_topk16_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, i64, vp, vp, vp, i64, vp, vp, vp,
+                                                   vp]
             L.dflash2_ref_ctx_gate.argtypes = [vp, i32, i64, i64, vp, i64, vp]
             L.dflash2_ref_pair_scores.argtypes = [i64, i32, vp, vp, vp, vp, vp, i32, i64, i32, vp, vp]
             L.dflash2_ref_walk.argtypes = [i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -128,6 +132,41 @@ def topk16(logits, params=None, rows_per_param=1, V=None, ld=None):
     mg = np.empty(rows, np.float64)
     lib().dflash2_ref_topk16(_p(raw), dt, rows, V, ld, _p(T), _p(tk), _p(tp), rows_per_param,
                              _p(idx), _p(U), _p(lse), _p(mg))
+    return idx, U, lse, mg
+
+
+SHARD_P = 64  # list entries per row of a shard partial
+
+
+def topk16_shard(logits, off, V_total, params=None, rows_per_param=1, P=SHARD_P):
+    """One vocabulary shard's partial.  logits [rows, Vs] hold tokens off..off+Vs-1.
+    Returns (part_idx [rows,P] i32, part_z [rows,P] f64, part_m [rows], part_s [rows])."""
+    raw, dt = _raw(logits)
+    rows, Vs = raw.shape
+    T, tk, tp = _params(params, rows)
+    idx = np.empty((rows, P), np.int32)
+    z = np.empty((rows, P), np.float64)
+    m = np.empty(rows, np.float64)
+    sm = np.empty(rows, np.float64)
+    lib().dflash2_ref_topk16_shard(_p(raw), dt, rows, Vs, Vs, off, V_total, _p(T), _p(tk), _p(tp),
+                                   rows_per_param, P, _p(idx), _p(z), _p(m), _p(sm))
+    return idx, z, m, sm
+
+
+def topk16_merge(part_idx, part_z, part_m, part_s, V_total, params=None, rows_per_param=1):
+    """Merge partials stacked [S, rows, P] / [S, rows].  Returns (cand_idx, cand_U, lse, margin)."""
+    pi = _arr(part_idx, np.int32)
+    pz = _arr(part_z, np.float64)
+    pm = _arr(part_m, np.float64)
+    ps = _arr(part_s, np.float64)
+    S, rows, P = pi.shape
+    T, tk, tp = _params(params, rows)
+    idx = np.empty((rows, NC), np.int32)
+    U = np.empty((rows, NC), np.float64)
+    lse = np.empty(rows, np.float64)
+    mg = np.empty(rows, np.float64)
+    lib().dflash2_ref_topk16_merge(S, rows, P, _p(pi), _p(pz), _p(pm), _p(ps), V_total, _p(T), _p(tk), _p(tp),
+                                   rows_per_param, _p(idx), _p(U), _p(lse), _p(mg))
     return idx, U, lse, mg
 
 

@@ -203,6 +203,159 @@ void dflash2_ref_topk16(const void *logits, int dtype, int64_t rows, int64_t V, 
 }
 
 /* ------------------------------------------------------------------------ */
+/* (1b) top-16 over a vocabulary split into shards: partials and merge.      */
+/* ------------------------------------------------------------------------ */
+/*
+ * A tensor-parallel LM head leaves each GPU the logits of one slice of the
+ * vocabulary.  The candidates and U of the whole row follow from one small
+ * partial per slice, exchanged once (a reading of this library: the pages
+ * run the drafter on one GPU with --tp 1).  Both functions restate the
+ * definitions of (1) over the union of the slices.
+ *
+ * Row length of a partial's list for parameters (T, top_k, top_p) and the
+ * whole vocabulary V_total: 16 for greedy and unfiltered rows, max(16, top_k)
+ * for rows filtered with 0 < top_k < V_total; rows whose filter needs more
+ * than P tokens (top_p < 1 with top_k off, or top_k > P) need the whole row
+ * and are not supported: their partials and merged outputs are -1 / NaN.
+ */
+static int shard_list_len(double T, int32_t tk, double tp, int64_t V_total, int P) {
+    if (T == 0.0) return NC;
+    int filtered = (tk > 0 && tk < V_total) || tp < 1.0;
+    if (!filtered) return NC;
+    if (tk == 0 || tk >= V_total || tk > P) return -1; /* needs the whole row */
+    return tk > NC ? tk : NC;
+}
+
+/*
+ * Partial of the shard holding tokens [off, off + Vs) of each row:
+ *   part_idx[r, i], part_z[r, i] (i < P): the shard's i-th token in the order
+ *     key, as a global id (off + v) and its logit, for i below the row's
+ *     list length (and below Vs); -1 and -inf after.
+ *   part_m[r]: the shard's largest logit; part_s[r]: the sum over the shard of
+ *     exp((z - part_m) / T'), T' = T for sampled rows and 1 for greedy rows;
+ *     0 for filtered rows (their merge uses the lists alone).
+ *   A shard row holding a NaN or +Inf, a row with invalid parameters and an
+ *   unsupported row: idx -1, m NaN, s NaN.  A shard row whose logits are all
+ *   -Inf is a slice of masked tokens: its list holds them (value -inf),
+ *   m = -inf, s = 0.
+ */
+void dflash2_ref_topk16_shard(const void *logits, int dtype, int64_t rows, int64_t Vs, int64_t ld,
+                              int64_t off, int64_t V_total, const float *temperature,
+                              const int32_t *top_k, const float *top_p, int64_t rows_per_param, int P,
+                              int32_t *part_idx, double *part_z, double *part_m, double *part_s) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; r++) {
+        const void *row = (const char *)logits + (size_t)(r * ld) * (dtype == REF_BF16 ? 2 : 4);
+        int64_t pi = rows_per_param > 0 ? r / rows_per_param : 0;
+        double T = temperature ? temperature[pi] : 0.0;
+        int32_t tk = top_k ? top_k[pi] : 0;
+        double tp = top_p ? top_p[pi] : 1.0;
+        for (int i = 0; i < P; i++) {
+            part_idx[r * P + i] = -1;
+            part_z[r * P + i] = -INFINITY;
+        }
+        int n = params_bad(T, tk, tp) ? -1 : shard_list_len(T, tk, tp, V_total, P);
+        int bad = n < 0;
+        for (int64_t v = 0; v < Vs && !bad; v++) {
+            double z = ref_load(row, dtype, v);
+            if (isnan(z) || (isinf(z) && z > 0)) bad = 1;
+        }
+        if (bad) {
+            part_m[r] = NAN;
+            part_s[r] = NAN;
+            continue;
+        }
+        entry *ord = sorted_row(row, dtype, Vs);
+        for (int i = 0; i < n && i < Vs; i++) {
+            part_idx[r * P + i] = (int32_t)(off + ord[i].id);
+            part_z[r * P + i] = ord[i].v;
+        }
+        double m = ord[0].v;
+        part_m[r] = m;
+        int filtered = T > 0.0 && ((tk > 0 && tk < V_total) || tp < 1.0);
+        double S = 0.0;
+        if (!filtered && !isinf(m)) {
+            double Tp = T > 0.0 ? T : 1.0;
+            for (int64_t i = 0; i < Vs; i++) S += exp((ord[i].v - m) / Tp);
+        }
+        part_s[r] = S;
+        free(ord);
+    }
+}
+
+/*
+ * Merge of S partials (part_* laid out [S, rows, P] and [S, rows]) into the
+ * row's cand_idx [rows, 16], cand_U and lse as (1) defines them for the whole
+ * row of V_total tokens: the union of the lists in the order key; for
+ * unfiltered rows lse = log sum_s exp(m_s / T') s_s (its largest term
+ * factored out) and U = z / T' - lse; for filtered rows the filter of (1) on
+ * the sorted union.  A row with a NaN partial, or none with a finite
+ * largest logit, and an unsupported row get -1 / NaN.
+ */
+void dflash2_ref_topk16_merge(int S, int64_t rows, int P, const int32_t *part_idx, const double *part_z,
+                              const double *part_m, const double *part_s, int64_t V_total,
+                              const float *temperature, const int32_t *top_k, const float *top_p,
+                              int64_t rows_per_param, int32_t *cand_idx, double *cand_U, double *lse,
+                              double *margin) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; r++) {
+        int64_t pi = rows_per_param > 0 ? r / rows_per_param : 0;
+        double T = temperature ? temperature[pi] : 0.0;
+        int32_t tk = top_k ? top_k[pi] : 0;
+        double tp = top_p ? top_p[pi] : 1.0;
+        if (margin) margin[r] = INFINITY;
+        int bad = params_bad(T, tk, tp) || shard_list_len(T, tk, tp, V_total, P) < 0;
+        double M = -INFINITY;
+        for (int s = 0; s < S && !bad; s++) {
+            double m = part_m[(int64_t)s * rows + r];
+            if (isnan(m)) bad = 1;
+            else if (m > M) M = m;
+        }
+        if (!bad && !isfinite(M)) bad = 1;
+        if (bad) {
+            for (int j = 0; j < NC; j++) {
+                cand_idx[r * NC + j] = -1;
+                cand_U[r * NC + j] = NAN;
+            }
+            lse[r] = NAN;
+            continue;
+        }
+        entry *u = (entry *)malloc((size_t)S * P * sizeof(entry));
+        int64_t n = 0;
+        for (int s = 0; s < S; s++)
+            for (int i = 0; i < P; i++) {
+                int64_t k = ((int64_t)s * rows + r) * P + i;
+                if (part_idx[k] < 0) continue;
+                u[n].v = part_z[k] == 0.0 ? 0.0 : part_z[k];
+                u[n].id = part_idx[k];
+                n++;
+            }
+        qsort(u, (size_t)n, sizeof(entry), entry_cmp);
+        for (int j = 0; j < NC; j++) cand_idx[r * NC + j] = j < n ? u[j].id : -1;
+        int filtered = T > 0.0 && ((tk > 0 && tk < V_total) || tp < 1.0);
+        if (!filtered) {
+            double Tp = T > 0.0 ? T : 1.0, sum = 0.0;
+            for (int s = 0; s < S; s++) {
+                double m = part_m[(int64_t)s * rows + r];
+                if (!isinf(m)) sum += part_s[(int64_t)s * rows + r] * exp((m - M) / Tp);
+            }
+            double L = M / Tp + log(sum);
+            lse[r] = L;
+            for (int j = 0; j < NC; j++) cand_U[r * NC + j] = j < n ? u[j].v / Tp - L : -INFINITY;
+        } else {
+            double *prob = (double *)malloc((size_t)n * sizeof(double));
+            double L, mg;
+            int64_t kept = ref_filter(u, n, T, tk, tp, prob, &L, &mg);
+            lse[r] = L;
+            if (margin) margin[r] = mg;
+            for (int j = 0; j < NC; j++) cand_U[r * NC + j] = (j < kept) ? u[j].v / T - L : -INFINITY;
+            free(prob);
+        }
+        free(u);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* (2) context gate H(h) = sigmoid(W_g h).                                   */
 /* ------------------------------------------------------------------------ */
 /* DFlash 2 proposer issue, "What upstream shipped" item 1 (context gate of
