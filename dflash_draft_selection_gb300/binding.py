@@ -53,6 +53,9 @@ def load_library():
         L.dflash2_topk16_noalloc.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, vp, vp, vp]
         L.dflash2_topk16_shard.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, i64, vp, vp, vp, vp, vp, sz, vp]
         L.dflash2_topk16_merge.argtypes = [i32, i64, vp, vp, vp, vp, i64, vp, i64, vp, vp, vp, vp]
+        L.dflash2_lmhead_topk16_workspace_bytes.argtypes = [i64, i64]
+        L.dflash2_lmhead_topk16_workspace_bytes.restype = sz
+        L.dflash2_lmhead_topk16.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, vp, vp, vp, sz, vp]
         L.dflash2_ctx_gate.argtypes = [vp, i32, i64, i64, vp, i32, vp, vp]
         L.dflash2_pair_score_walk.argtypes = [i64, i32, vp, vp, vp, vp, vp, i32, i64, i32, vp, vp, vp, vp, vp,
                                               vp, vp, vp]
@@ -66,6 +69,7 @@ def load_library():
         L.dflash2_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
         L.dflash2_test_hold.argtypes = [vp, i64]
         for fn in ("dflash2_topk16", "dflash2_topk16_noalloc", "dflash2_topk16_shard", "dflash2_topk16_merge",
+                   "dflash2_lmhead_topk16",
                    "dflash2_ctx_gate", "dflash2_pair_score_walk",
                    "dflash2_verify", "dflash2_conv2tap", "dflash2_device_error", "dflash2_test_hold"):
             getattr(L, fn).restype = i32
@@ -141,6 +145,10 @@ class Workspace:
     @staticmethod
     def for_topk16(rows: int, device="cuda") -> "Workspace":
         return Workspace(load_library().dflash2_topk16_workspace_bytes(rows), device)
+
+    @staticmethod
+    def for_lmhead(rows: int, V: int, device="cuda") -> "Workspace":
+        return Workspace(load_library().dflash2_lmhead_topk16_workspace_bytes(rows, V), device)
 
     @staticmethod
     def for_verify(B: int, K: int, device="cuda") -> "Workspace":
@@ -232,6 +240,28 @@ def topk16_merge(part_idx, part_z, part_m, part_s, V_total: int, params=None, ro
     _check("dflash2_topk16_merge",
            L.dflash2_topk16_merge(S, rows, _ptr(part_idx), _ptr(part_z), _ptr(part_m), _ptr(part_s), V_total,
                                   _ptr(p), rows_per_param, _ptr(cand_idx), _ptr(cand_U), _ptr(lse), _stream(dev)))
+    return cand_idx, cand_U, lse
+
+
+def lmhead_topk16(h: torch.Tensor, W: torch.Tensor, params=None, rows_per_param: int = 1, ws=None, out=None):
+    """dflash2_lmhead_topk16: h [rows, hidden] bf16, W [V, hidden] bf16.  Returns (cand_idx, cand_U, lse)."""
+    L = load_library()
+    _need_cuda(h, W)
+    assert h.dtype == torch.bfloat16 and W.dtype == torch.bfloat16 and h.is_contiguous() and W.is_contiguous()
+    rows, hidden = h.shape
+    V = W.shape[0]
+    dev = h.device
+    if out is None:
+        out = (torch.empty(rows, NC, dtype=torch.int32, device=dev),
+               torch.empty(rows, NC, dtype=torch.float32, device=dev),
+               torch.empty(rows, dtype=torch.float32, device=dev))
+    cand_idx, cand_U, lse = out
+    if ws is None:
+        ws = Workspace.for_lmhead(rows, V, dev)
+    p = _params_from(params, dev)
+    _check("dflash2_lmhead_topk16",
+           L.dflash2_lmhead_topk16(_ptr(h), _ptr(W), rows, hidden, V, _ptr(p), rows_per_param, _ptr(cand_idx),
+                                   _ptr(cand_U), _ptr(lse), ws.ptr(), ws.nbytes, _stream(dev)))
     return cand_idx, cand_U, lse
 
 

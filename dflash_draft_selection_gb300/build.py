@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdflash2.so")
-SOURCES = ["topk16.cu", "verify.cu", "walk.cu", "gate.cu", "conv.cu", "api.cu"]
+SOURCES = ["topk16.cu", "verify.cu", "walk.cu", "gate.cu", "lmhead.cu", "conv.cu", "api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -7,6 +7,7 @@ namespace dfl {
 unsigned int read_error_topk(bool clear);
 unsigned int read_error_verify(bool clear);
 unsigned int read_error_gate(bool clear);
+unsigned int read_error_lmhead(bool clear);
 
 // dflash2_test_hold's setting: read by every scan launch (make_geom).
 static std::mutex g_hold_mu;
@@ -45,6 +46,6 @@ extern "C" dflash2_status dflash2_device_error(uint32_t *code, int clear) {
     if (!code) return DFLASH2_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return DFLASH2_ERR_CUDA;
     *code = dfl::read_error_topk(clear != 0) | dfl::read_error_verify(clear != 0) |
-            dfl::read_error_gate(clear != 0);
+            dfl::read_error_gate(clear != 0) | dfl::read_error_lmhead(clear != 0);
     return cudaPeekAtLastError() == cudaSuccess ? DFLASH2_OK : DFLASH2_ERR_CUDA;
 }

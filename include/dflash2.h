@@ -193,6 +193,31 @@ dflash2_status dflash2_topk16_merge(int32_t S, int64_t rows, const int32_t *part
                                     float *cand_U, float *lse, dflash2_stream stream);
 
 /*
+ * dflash2_lmhead_topk16 -- the drafter's LM head fused with dflash2_topk16:
+ * [P] "What upstream shipped" item 1 (keep the top-16 candidates of each
+ * drafted position) and [F] Runtime (16 candidates per slot from the LM
+ * head), with the logits z = h . W^T never written to memory.  The GEMM runs
+ * on the tensor cores (bf16 inputs, fp32 accumulation); the candidates, U
+ * and lse are those of dflash2_topk16 on the fp32 logits.
+ *
+ * h [rows, hidden] bf16 and W [V, hidden] bf16, row-major (W is the LM head's
+ * weight, one row per token).  hidden a multiple of 64.  params and
+ * rows_per_param as for dflash2_topk16.  Rows that would need more than 16
+ * candidates (a top_k filter above 16) or the whole row (top_p with top_k
+ * off) get -1 / NaN.
+ * ws: dflash2_lmhead_topk16_workspace_bytes(rows, V) bytes, for the current
+ *   device (the per-row partials of each CTA's vocabulary range, combined by
+ *   dflash2_topk16_merge on the same stream).
+ * Errors: INVALID_ARG for NULL or misaligned pointers, rows < 0, hidden not a
+ * positive multiple of 64, V < 16 or V >= 2^31, rows_per_param < 1;
+ * WORKSPACE if ws_bytes is too small.
+ */
+size_t dflash2_lmhead_topk16_workspace_bytes(int64_t rows, int64_t V);
+dflash2_status dflash2_lmhead_topk16(const void *h, const void *W, int64_t rows, int64_t hidden, int64_t V,
+                                     const dflash2_sampling *params, int64_t rows_per_param, int32_t *cand_idx,
+                                     float *cand_U, float *lse, void *ws, size_t ws_bytes, dflash2_stream stream);
+
+/*
  * dflash2_ctx_gate -- [P] item 1 "context gate" of the bilinear selector,
  * taken as gate = sigmoid(W_g h) with no bias.
  *

@@ -48,6 +48,8 @@ def lib():
                                                    vp, vp]
             L.dflash2_ref_topk16_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, i64, vp, vp, vp, i64, vp, vp, vp,
                                                    vp]
+            L.dflash2_ref_lmhead_topk16.argtypes = [vp, vp, i32, i64, i64, i64, vp, vp, vp, i64, vp, vp, vp, vp,
+                                                    vp]
             L.dflash2_ref_ctx_gate.argtypes = [vp, i32, i64, i64, vp, i64, vp]
             L.dflash2_ref_pair_scores.argtypes = [i64, i32, vp, vp, vp, vp, vp, i32, i64, i32, vp, vp]
             L.dflash2_ref_walk.argtypes = [i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -168,6 +170,24 @@ def topk16_merge(part_idx, part_z, part_m, part_s, V_total, params=None, rows_pe
     lib().dflash2_ref_topk16_merge(S, rows, P, _p(pi), _p(pz), _p(pm), _p(ps), V_total, _p(T), _p(tk), _p(tp),
                                    rows_per_param, _p(idx), _p(U), _p(lse), _p(mg))
     return idx, U, lse, mg
+
+
+def lmhead_topk16(h, W, params=None, rows_per_param=1):
+    """h [rows, hidden], W [V, hidden] (bf16 or f32).  Returns (cand_idx, cand_U, lse, margin, gap)."""
+    hr, dt = _raw(h)
+    wr, dt2 = _raw(W)
+    assert dt == dt2
+    rows, hidden = hr.shape
+    V = wr.shape[0]
+    T, tk, tp = _params(params, rows)
+    idx = np.empty((rows, NC), np.int32)
+    U = np.empty((rows, NC), np.float64)
+    lse = np.empty(rows, np.float64)
+    mg = np.empty(rows, np.float64)
+    gap = np.empty(rows, np.float64)
+    lib().dflash2_ref_lmhead_topk16(_p(hr), _p(wr), dt, rows, hidden, V, _p(T), _p(tk), _p(tp), rows_per_param,
+                                    _p(idx), _p(U), _p(lse), _p(mg), _p(gap))
+    return idx, U, lse, mg, gap
 
 
 def ctx_gate(h, Wg):

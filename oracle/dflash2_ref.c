@@ -158,6 +158,32 @@ static int64_t ref_filter(const entry *ord, int64_t V, double T, int32_t top_k, 
  * margin[r] (optional) = top_p decision margin of the row (inf if none).
  * Unusable rows and invalid parameters give idx -1, U NaN, lse NaN.
  */
+/* The outputs of (1) for one usable row whose V entries are sorted by the
+ * order key: idx/U are the row's 16 slots, *lse its normaliser, *margin its
+ * top_p decision margin (inf when none). */
+static void topk16_sorted(const entry *ord, int64_t V, double T, int32_t tk, double tp, int32_t *idx, double *U,
+                          double *lse, double *margin) {
+    for (int j = 0; j < NC; j++) idx[j] = ord[j].id;
+    int filtered = T > 0.0 && ((tk > 0 && tk < V) || tp < 1.0);
+    *margin = INFINITY;
+    if (!filtered) {
+        double Tp = T > 0.0 ? T : 1.0;
+        double M = ord[0].v / Tp, S = 0.0;
+        for (int64_t i = 0; i < V; i++) S += exp(ord[i].v / Tp - M);
+        double L = M + log(S);
+        *lse = L;
+        for (int j = 0; j < NC; j++) U[j] = ord[j].v / Tp - L;
+    } else {
+        double *prob = (double *)malloc((size_t)V * sizeof(double));
+        double L, mg;
+        int64_t kept = ref_filter(ord, V, T, tk, tp, prob, &L, &mg);
+        *lse = L;
+        *margin = mg;
+        for (int j = 0; j < NC; j++) U[j] = (j < kept) ? ord[j].v / T - L : -INFINITY;
+        free(prob);
+    }
+}
+
 void dflash2_ref_topk16(const void *logits, int dtype, int64_t rows, int64_t V, int64_t ld,
                         const float *temperature, const int32_t *top_k, const float *top_p,
                         int64_t rows_per_param, int32_t *cand_idx, double *cand_U, double *lse,
@@ -179,25 +205,9 @@ void dflash2_ref_topk16(const void *logits, int dtype, int64_t rows, int64_t V, 
             continue;
         }
         entry *ord = sorted_row(row, dtype, V);
-        for (int j = 0; j < NC; j++) cand_idx[r * NC + j] = ord[j].id;
-        int filtered = T > 0.0 && ((tk > 0 && tk < V) || tp < 1.0);
-        if (!filtered) {
-            double Tp = T > 0.0 ? T : 1.0;
-            double M = ord[0].v / Tp, S = 0.0;
-            for (int64_t i = 0; i < V; i++) S += exp(ord[i].v / Tp - M);
-            double L = M + log(S);
-            lse[r] = L;
-            for (int j = 0; j < NC; j++) cand_U[r * NC + j] = ord[j].v / Tp - L;
-        } else {
-            double *prob = (double *)malloc((size_t)V * sizeof(double));
-            double L, mg;
-            int64_t kept = ref_filter(ord, V, T, tk, tp, prob, &L, &mg);
-            lse[r] = L;
-            if (margin) margin[r] = mg;
-            for (int j = 0; j < NC; j++)
-                cand_U[r * NC + j] = (j < kept) ? ord[j].v / T - L : -INFINITY;
-            free(prob);
-        }
+        double mg;
+        topk16_sorted(ord, V, T, tk, tp, cand_idx + r * NC, cand_U + r * NC, lse + r, &mg);
+        if (margin) margin[r] = mg;
         free(ord);
     }
 }
@@ -352,6 +362,61 @@ void dflash2_ref_topk16_merge(int S, int64_t rows, int P, const int32_t *part_id
             free(prob);
         }
         free(u);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* (1c) the LM head and the top-16 in one: z = h . W^T, then (1).            */
+/* ------------------------------------------------------------------------ */
+/*
+ * DFlash 2 proposer issue, "What upstream shipped" item 1 and FreeToken PR
+ * 857 "Details"/Runtime (the candidates come from the LM head): the logits
+ * of row r are z_v = sum_k h[r,k] W[v,k] (bf16 inputs, exact fp64 products
+ * and sums), and the outputs are those of (1) on them.  Rows that would need
+ * more than 16 candidates (a top_k filter above 16) or the whole row (top_p
+ * with top_k off) get -1 / NaN, as the library's fused kernel gives them.
+ * gap[r] (optional): the smallest difference between consecutive logits
+ * among the row's 17 best, the margin of the candidates' order.
+ */
+void dflash2_ref_lmhead_topk16(const void *h, const void *W, int dtype, int64_t rows, int64_t hidden, int64_t V,
+                               const float *temperature, const int32_t *top_k, const float *top_p,
+                               int64_t rows_per_param, int32_t *cand_idx, double *cand_U, double *lse,
+                               double *margin, double *gap) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < rows; r++) {
+        int64_t pi = rows_per_param > 0 ? r / rows_per_param : 0;
+        double T = temperature ? temperature[pi] : 0.0;
+        int32_t tk = top_k ? top_k[pi] : 0;
+        double tp = top_p ? top_p[pi] : 1.0;
+        if (margin) margin[r] = INFINITY;
+        if (gap) gap[r] = INFINITY;
+        int need = T == 0.0 || !((tk > 0 && tk < V) || tp < 1.0) ? NC : ((tk == 0 || tk >= V) ? -1 : tk);
+        entry *ord = (entry *)malloc((size_t)V * sizeof(entry));
+        int bad = params_bad(T, tk, tp) || need < 0 || need > NC;
+        for (int64_t v = 0; v < V && !bad; v++) {
+            double z = 0.0;
+            for (int64_t k = 0; k < hidden; k++) z += ref_load(h, dtype, r * hidden + k) * ref_load(W, dtype, v * hidden + k);
+            if (isnan(z) || isinf(z)) bad = 1;
+            ord[v].v = z == 0.0 ? 0.0 : z;
+            ord[v].id = (int32_t)v;
+        }
+        if (bad) {
+            for (int j = 0; j < NC; j++) {
+                cand_idx[r * NC + j] = -1;
+                cand_U[r * NC + j] = NAN;
+            }
+            lse[r] = NAN;
+            free(ord);
+            continue;
+        }
+        qsort(ord, (size_t)V, sizeof(entry), entry_cmp);
+        double mg;
+        topk16_sorted(ord, V, T, tk, tp, cand_idx + r * NC, cand_U + r * NC, lse + r, &mg);
+        if (margin) margin[r] = mg;
+        if (gap)
+            for (int j = 0; j < NC && j + 1 < V; j++)
+                if (ord[j].v - ord[j + 1].v < gap[r]) gap[r] = ord[j].v - ord[j + 1].v;
+        free(ord);
     }
 }
 
