@@ -74,4 +74,11 @@ inline int esize(dflash2_dtype dt) { return dt == DFLASH2_BF16 ? 2 : 4; }
 
 inline bool dtype_ok(dflash2_dtype dt) { return dt == DFLASH2_BF16 || dt == DFLASH2_F32; }
 
+// The merge of partials whose lists hold at most 16 entries (topk16.cu); the
+// fused LM head's second launch.
+dflash2_status launch_merge16(int S, int64_t rows, const int32_t *part_idx, const float *part_z, const float *part_m,
+                              const float *part_s, int64_t V_total, const dflash2_sampling *params,
+                              int64_t rows_per_param, int32_t *cand_idx, float *cand_U, float *lse,
+                              cudaStream_t stream);
+
 }  // namespace dfl

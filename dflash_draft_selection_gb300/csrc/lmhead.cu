@@ -18,7 +18,7 @@
 // thread) drain the other accumulator: running max and sum of exponentials,
 // and a sorted list of the row's 16 best logits.  At the end of its range a
 // CTA writes, per row, a partial in the layout of dflash2_topk16_shard (the
-// range is a vocabulary slice); dflash2_topk16_merge combines the ranges.
+// range is a vocabulary slice); a second kernel merges the ranges' partials.
 //
 // Waits are bounded: a timed-out wait sets the error word and the CTA's rows
 // come out -1 / NaN.
@@ -34,7 +34,8 @@ constexpr int LBM = 128;   // rows of a tile (tensor-memory lanes)
 constexpr int LBN = 256;   // vocabulary entries of a tile (accumulator columns)
 constexpr int LBK = 64;    // hidden elements per stage (one 128-byte swizzle row)
 constexpr int LSTAGES = 4;
-constexpr int LM_THREADS = 192;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+constexpr int LM_THREADS = 224;  // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer, 6 L2 prefetch
+constexpr int LM_PF = 12;        // k-blocks of W asked of L2 ahead of the producer (~3 us of MMA)
 constexpr int LM_TOP = 16;       // candidates kept per row and range
 constexpr long long LM_WAIT = 4000000000ll;   // ~2 s
 constexpr long long LM_DRAIN = 200000000ll;   // ~0.1 s
@@ -49,6 +50,7 @@ struct LmSmem {
     uint64_t done;
     uint32_t tmem_base;
     int abort_flag;
+    int issued;  // k-blocks the producer has copied so far
 };
 
 static_assert(sizeof(LmSmem) + 1024 <= 227 * 1024, "the LM-head pipeline fits one SM's shared memory");
@@ -58,6 +60,8 @@ struct LmArgs {
     int kblocks;      // hidden / 64
     int ntiles;       // N tiles of the vocabulary
     int nranges;      // N ranges per M tile (= partials per row)
+    int mtiles;       // M tiles
+    const char *W;    // the LM head's weight (for the L2 prefetch)
     const dflash2_sampling *params;
     int64_t rows_per_param;
     int32_t *part_idx;  // [nranges, rows, DFLASH2_SHARD_LIST]
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(LM_THREADS, 1) k_lmhead(const __grid_constant_
         }
         mbar_init(&sm.done, 1);
         sm.abort_flag = 0;
+        sm.issued = 0;
         fence_barrier_init();
     }
     if (warp == 5) tmem_alloc(&sm.tmem_base, 512);
@@ -192,11 +197,33 @@ __global__ void __launch_bounds__(LM_THREADS, 1) k_lmhead(const __grid_constant_
                     mbar_arrive_expect_tx(&sm.full[s], (LBM + LBN) * LBK * 2);
                     tma_load_2d(sm.a[s], &tm_h, kb * LBK, mt * LBM, &sm.full[s]);
                     tma_load_2d(sm.b[s], &tm_w, kb * LBK, (t0 + j) * LBN, &sm.full[s]);
+                    *reinterpret_cast<volatile int *>(&sm.issued) = it + 1;
                 }
             }
             // Leave no copy in flight into this CTA's shared memory.
             for (int i = it > LSTAGES ? it - LSTAGES : 0; i < it; ++i)
                 mbar_wait(&sm.full[i % LSTAGES], (i / LSTAGES) & 1, LM_DRAIN);
+        }
+    } else if (warp == 6) {
+        // L2 prefetch of W, LM_PF k-blocks ahead of the producer: the copies of
+        // a range's W tiles then find them in L2 instead of waiting on HBM.  The
+        // range's CTAs (one per M tile) share the work: this CTA takes rows
+        // mt, mt + mtiles, ... of each tile's k-block, one 128-byte line each.
+        const int total = nt * a.kblocks;
+        const int64_t ld = static_cast<int64_t>(a.kblocks) * LBK * 2;  // bytes per W row
+        const long long tstart = clock64();
+        for (int i = 0; i < total && !lm_aborted(sm); ++i) {
+            while (i >= *reinterpret_cast<volatile int *>(&sm.issued) + LM_PF) {
+                if (lm_aborted(sm) || clock64() - tstart > LM_WAIT) break;
+                __nanosleep(200);
+            }
+            if (lm_aborted(sm) || clock64() - tstart > LM_WAIT) break;
+            const int64_t n0 = static_cast<int64_t>(t0 + i / a.kblocks) * LBN;
+            const int kb = i % a.kblocks;
+            for (int rr = mt + lane * a.mtiles; rr < LBN; rr += 32 * a.mtiles) {
+                const int64_t v = n0 + rr;
+                if (v < a.V) asm volatile("prefetch.global.L2 [%0];" ::"l"(a.W + v * ld + kb * LBK * 2));
+            }
         }
     } else if (warp == 5) {
         // MMA issuer
@@ -358,6 +385,8 @@ extern "C" dflash2_status dflash2_lmhead_topk16(const void *h, const void *W, in
     a.kblocks = static_cast<int>(hidden / LBK);
     a.ntiles = static_cast<int>((V + LBN - 1) / LBN);
     a.nranges = nranges;
+    a.mtiles = static_cast<int>((rows + LBM - 1) / LBM);
+    a.W = static_cast<const char *>(W);
     a.params = params;
     a.rows_per_param = rows_per_param;
     const size_t lists = static_cast<size_t>(nranges) * rows * DFLASH2_SHARD_LIST;
@@ -389,6 +418,6 @@ extern "C" dflash2_status dflash2_lmhead_topk16(const void *h, const void *W, in
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, k_lmhead, tm_h, tm_w, a) != cudaSuccess) return DFLASH2_ERR_CUDA;
     if (after_launch() != DFLASH2_OK) return DFLASH2_ERR_CUDA;
-    return dflash2_topk16_merge(nranges, rows, a.part_idx, a.part_z, a.part_m, a.part_s, V, params, rows_per_param,
-                                cand_idx, cand_U, lse, stream);
+    return launch_merge16(nranges, rows, a.part_idx, a.part_z, a.part_m, a.part_s, V, params, rows_per_param,
+                          cand_idx, cand_U, lse, s);
 }

@@ -137,6 +137,95 @@ __global__ void __launch_bounds__(256) k_topk16_merge(int S, int64_t rows, const
     finalize_draft<2>(res, task, row, cand_idx, cand_U, lse, lane);
 }
 
+// Merge of S partials whose lists hold at most 16 entries (the fused LM
+// head's, one per vocabulary range), one warp per row: each lane combines
+// the log normalisers of shards lane, lane + 32, ... and the lanes combine in
+// a fixed butterfly; the S * 16 candidate keys are loaded 256 at a time (all
+// loads in flight at once) and sorted into the row's list 32 at a time.
+__global__ void __launch_bounds__(256) k_topk16_merge16(int S, int64_t rows, const int32_t *part_idx,
+                                                        const float *part_z, const float *part_m,
+                                                        const float *part_s, int64_t V_total,
+                                                        const dflash2_sampling *params, int64_t rows_per_param,
+                                                        int32_t *cand_idx, float *cand_U, float *lse) {
+    const int lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_trigger();
+    if (row >= rows) return;
+    const RowTask task = decode_row(params, row / rows_per_param, V_total, false);
+    const float c = LOG2E / task.T;
+    float m = NEG_INF, sm = 0.0f;
+    bool bad = task.mode == MODE_SKIP;
+    for (int sh = lane; sh < S; sh += 32) {
+        const float m2 = part_m[static_cast<int64_t>(sh) * rows + row];
+        const float s2 = part_s[static_cast<int64_t>(sh) * rows + row];
+        if (m2 != m2) bad = true;
+        else lse_combine(m, sm, m2, s2, c);
+    }
+    bad = __any_sync(FULL, bad);
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) {
+        const float m2 = __shfl_xor_sync(FULL, m, d);
+        const float s2 = __shfl_xor_sync(FULL, sm, d);
+        lse_combine(m, sm, m2, s2, c);
+    }
+    WarpList<1> acc;
+    acc.clear();
+    const int n = S * 16;
+    for (int base = 0; base < n; base += 8 * 32) {
+        uint64_t k[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int e = base + u * 32 + lane;
+            const int64_t o = (static_cast<int64_t>(e >> 4) * rows + row) * DFLASH2_SHARD_LIST + (e & 15);
+            const int32_t id = e < n ? part_idx[o] : -1;
+            const float z = e < n ? part_z[o] : NEG_INF;
+            k[u] = id >= 0 ? make_key(z, static_cast<uint32_t>(id)) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (!__any_sync(FULL, k[u] != 0)) continue;
+            WarpList<1> o;
+            o.k[0] = warp_sort_desc(k[u], lane);
+            acc.merge(o, lane);
+        }
+    }
+    if (task.mode == MODE_SKIP || task.mode == MODE_ARGMAX || task.nsel > 16) {
+        if (lane < NC) {
+            cand_idx[row * NC + lane] = -1;
+            cand_U[row * NC + lane] = NAN;
+        }
+        if (lane == 0) lse[row] = NAN;
+        return;
+    }
+    RowResult<1> res;
+    res.list = acc;
+    res.best = 0;
+    res.m = m;
+    res.s = sm;
+    res.bad = bad;
+    finalize_draft<1>(res, task, row, cand_idx, cand_U, lse, lane);
+}
+
+dflash2_status launch_merge16(int S, int64_t rows, const int32_t *part_idx, const float *part_z, const float *part_m,
+                              const float *part_s, int64_t V_total, const dflash2_sampling *params,
+                              int64_t rows_per_param, int32_t *cand_idx, float *cand_U, float *lse,
+                              cudaStream_t stream) {
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 0x7fffffff) return DFLASH2_ERR_UNSUPPORTED;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1] = {pdl_attribute()};
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_topk16_merge16, S, rows, part_idx, part_z, part_m, part_s, V_total, params,
+                           rows_per_param, cand_idx, cand_U, lse) != cudaSuccess)
+        return DFLASH2_ERR_CUDA;
+    return after_launch();
+}
+
 // SAMPLED: some request may sample (params given): lists of 64 keys and every
 // row mode; otherwise every row is greedy (top-16 and the log normaliser).
 // Warps 0..SCAN_WARPS-1 stream the CTA's rows; the last warp completes each
