@@ -320,6 +320,7 @@ def run_ours(args, rank, world, local):
             if name != args.config:
                 aux[name] = time_workload(name, dev, peak, peak_kind)
         aux["conv2tap"] = time_conv(dev, peak)
+        aux["lmhead_topk16"] = time_lmhead(dev)
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -417,6 +418,46 @@ def time_workload(name, dev, peak, peak_kind, steps=30):
            "value": round(shp.B / (ms_per_step * 1e-3), 1), "unit": UNIT, "ms_per_step": round(ms_per_step, 5),
            "steps": reps * nsets, "roofline": roofline(kern, algo, ms_per_step, peak, peak_kind, name)}
     del chain, g
+    torch.cuda.empty_cache()
+    return out
+
+
+def time_lmhead(dev, reps=10):
+    """dflash2_lmhead_topk16 (the drafter's LM head fused with the top-16) at the 27B drafter's shape
+    (hidden 5120, V 151936) for 448 rows (B=64, K=7) and 3840 rows (B=256, K=15): mean of `reps`
+    launches with CUDA events (W is 1.56 GB, larger than L2); algorithmic FLOPs 2 * rows * hidden * V
+    against the measured bf16 tensor peak (burst: the kernel is timed alone)."""
+    import torch
+
+    import dflash_draft_selection_gb300 as d2
+    peaks = {}
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        peaks = json.load(open(p))
+    peak = float(peaks.get("bf16_tflops", 1900.0))
+    out = {"unit": "TFLOP/s", "peak": peak, "bound": "tensor", "peak_source": "measured" if peaks else "fallback"}
+    g = torch.Generator(device=dev).manual_seed(11)
+    hidden, V = 5120, 151936
+    W = (torch.randn(V, hidden, generator=g, device=dev) / hidden ** 0.5).bfloat16()
+    for rows in (448, 3840):
+        h = torch.randn(rows, hidden, generator=g, device=dev).bfloat16()
+        ws = d2.Workspace.for_lmhead(rows, V, dev)
+        res = (torch.empty(rows, 16, dtype=torch.int32, device=dev), torch.empty(rows, 16, device=dev),
+               torch.empty(rows, device=dev))
+        for _ in range(3):
+            d2.lmhead_topk16(h, W, ws=ws, out=res)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            d2.lmhead_topk16(h, W, ws=ws, out=res)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        tf = 2.0 * rows * hidden * V / (us * 1e-6) / 1e12
+        out[f"rows_{rows}"] = {"avg_launch_us": round(us, 1), "achieved": round(tf, 1), "frac": round(tf / peak, 4)}
+        del h, ws
+    del W
     torch.cuda.empty_cache()
     return out
 
