@@ -230,7 +230,6 @@ __global__ void __launch_bounds__(LM_THREADS, 1) k_lmhead(const __grid_constant_
         if (lane == 0) {
             const uint32_t idesc = lm_idesc();
             int it = 0;
-            bool issued_any = false;
             for (int j = 0; j < nt && !lm_aborted(sm); ++j) {
                 const int b = j & 1;
                 if (j >= 2 && !mbar_wait(&sm.acc_empty[b], ((j >> 1) - 1) & 1, LM_WAIT)) {
@@ -252,7 +251,6 @@ __global__ void __launch_bounds__(LM_THREADS, 1) k_lmhead(const __grid_constant_
                     for (int k = 0; k < LBK / 16; ++k)  // 16 bf16 = 32 bytes per MMA: +2 in the address field
                         mma_bf16(tmem + static_cast<uint32_t>(b * LBN), ad + 2 * k, bd + 2 * k, idesc, kb > 0 || k > 0);
                     mma_commit(&sm.empty[s]);
-                    issued_any = true;
                 }
                 if (!ok) {
                     lm_abort(sm);
@@ -263,7 +261,6 @@ __global__ void __launch_bounds__(LM_THREADS, 1) k_lmhead(const __grid_constant_
             // Every MMA issued has completed once this commit arrives.
             mma_commit(&sm.done);
             mbar_wait(&sm.done, 0, LM_DRAIN);
-            (void)issued_any;
         }
     } else {
         // Epilogue: thread = row w*32 + lane of the tile.
