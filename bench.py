@@ -315,11 +315,10 @@ def run_ours(args, rank, world, local):
     # ---- the other workloads (sampled; stress) and the drafter-side conv, each with its own roofline ----
     aux = None
     if not args.no_kernel_pass:
-        aux = {}
+        aux = {"conv2tap": time_conv(dev, peak)}
         for name in AUX_WORKLOADS:
             if name != args.config:
                 aux[name] = time_workload(name, dev, peak, peak_kind)
-        aux["conv2tap"] = time_conv(dev, peak)
         aux["lmhead_topk16"] = time_lmhead(dev)
 
     # ---- end to end through the public API with host buffers ----
@@ -492,30 +491,48 @@ def time_conv(dev, peak, reps=50):
 
 
 def run_e2e(chain, shp, dev, stream, steps, world):
-    """Host-resident inputs: H2D copies + the four calls + D2H of the result, every step."""
+    """Host-resident inputs through the public calls: every step copies its inputs from pinned host
+    memory (cudaMemcpyAsync on a copy stream), runs the four calls and copies its result back to the
+    host.  Two device input sets alternate, so step i + 1's copy runs while step i computes (the copy
+    is the bound: ~210 GB/s host to device); the clock stops when the last result is on the host."""
     import torch
-    base = chain.sets[0]
     names = ["draft_logits", "target_logits", "h", "last_tok"] + (["u_walk", "u_acc", "u_res"] if chain.sampled else [])
+    base = chain.sets[0]
     host = {n: getattr(base, n).cpu().pin_memory() for n in names}
     h2d = sum(t.numel() * t.element_size() for t in host.values())
-    res_host = [torch.empty_like(chain.acc, device="cpu").pin_memory(), torch.empty_like(chain.out, device="cpu").pin_memory(),
-                torch.empty_like(chain.st, device="cpu").pin_memory()]
-    d2h = sum(t.numel() * t.element_size() for t in res_host)
-    dst = chain.sets[0]
-    for i in range(steps + 3):
+    dsets = chain.sets[:2]
+    res_host = [(torch.empty_like(chain.acc, device="cpu").pin_memory(),
+                 torch.empty_like(chain.out, device="cpu").pin_memory(),
+                 torch.empty_like(chain.st, device="cpu").pin_memory()) for _ in range(2)]
+    d2h = sum(t.numel() * t.element_size() for t in res_host[0])
+    copy = torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
+    t0 = None
+    total = steps + 3
+    for i in range(total):
         if i == 3:
             torch.cuda.synchronize()
             t0 = time.perf_counter()
-        for n in names:
-            getattr(dst, n).copy_(host[n], non_blocking=True)
+        k = i % 2
+        dst = dsets[k]
+        with torch.cuda.stream(copy):
+            if i >= 2:
+                copy.wait_event(consumed[k])        # step i - 2 has finished with this set
+            for n in names:
+                getattr(dst, n).copy_(host[n], non_blocking=True)
+            copied[k].record(copy)
+        stream.wait_event(copied[k])
         chain.run(dst)
-        res_host[0].copy_(chain.acc, non_blocking=True)
-        res_host[1].copy_(chain.out, non_blocking=True)
-        res_host[2].copy_(chain.st, non_blocking=True)
-        stream.synchronize()
+        for t_h, t_d in zip(res_host[k], (chain.acc, chain.out, chain.st)):
+            t_h.copy_(t_d, non_blocking=True)
+        consumed[k].record(stream)
+    stream.synchronize()
+    copy.synchronize()
     dt = max_over_ranks(time.perf_counter() - t0, dev, world)
     return {"value": round(whole_job_rate(shp.B, world, steps, dt), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4)}
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(dt / steps * 1e3, 4),
+            "pipelining": "two input sets: step i+1's host-to-device copy overlaps step i"}
 
 
 # ----------------------------------------------------------- CPU oracle ----
