@@ -308,6 +308,7 @@ struct RowTask {
     int status;   // DFLASH2_ST_* reason for MODE_SKIP
     float T;      // temperature of the distribution (1 for greedy draft rows)
     float top_p;
+    bool wide;    // a draft row whose filter may reach past its 64 best (top_k > 64, or top_p with top_k off)
 };
 
 // Decide how a row is scanned.  `target` rows need the target distribution
@@ -315,6 +316,7 @@ struct RowTask {
 __device__ __forceinline__ RowTask decode_row(const dflash2_sampling *P, int64_t pidx, int64_t V,
                                               bool target) {
     RowTask t;
+    t.wide = false;
     t.ek = static_cast<int>(V);
     t.status = DFLASH2_ST_OK;
     t.top_p = 1.0f;
@@ -354,6 +356,13 @@ __device__ __forceinline__ RowTask decode_row(const dflash2_sampling *P, int64_t
         return t;
     }
     if (ek > DFLASH2_MAX_TOPK) {
+        if (!target) {  // draft: the 64 best and the log normaliser; the cut may need further passes
+            t.mode = MODE_TOPN_LSE;
+            t.nsel = DFLASH2_MAX_TOPK;
+            t.ek = static_cast<int>(ek);
+            t.wide = true;
+            return t;
+        }
         t.mode = MODE_SKIP;
         t.nsel = 0;
         t.status = DFLASH2_ST_UNSUPPORTED;

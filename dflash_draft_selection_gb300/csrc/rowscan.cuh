@@ -154,6 +154,10 @@ struct ScanSmem {
         unsigned int ring_end[SCAN_WARPS];  // 1 + the warp's ring count at its end of the row; 0 before
     } hand[2];
     alignas(16) unsigned char scratch[GCAP * 8];  // the completion warp's gathered keys; verify's draws
+    struct WideHist {                             // the completion warp's histogram for wide rows
+        double mass[256];                         // fp64: a bin may sum 10^5 weights
+        unsigned int cnt[256];
+    } wide;
     alignas(128) unsigned char buf[SCAN_WARPS][WSTAGES][CHUNK_BYTES];
 };
 

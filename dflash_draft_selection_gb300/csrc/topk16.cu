@@ -8,14 +8,18 @@
 #include "host.hpp"
 #include "rowscan.cuh"
 #include "filter.cuh"
+#include "wide.cuh"
 
 namespace dfl {
 
 static __device__ unsigned int g_err_topk;
 
+// The row's candidates, U and lse.  A wide row (wc non-NULL) keeps the first
+// wc->cut tokens in the order key, of mass wc->P relative to the row maximum.
 template <int R>
 __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const RowTask &task, int64_t row,
-                               int32_t *cand_idx, float *cand_U, float *lse, int lane) {
+                               int32_t *cand_idx, float *cand_U, float *lse, int lane,
+                               const WideCut *wc = nullptr) {
     const uint64_t k = res.list.k[0];
     const float z = key_val(k);
     int32_t idx = key_idx(k);
@@ -23,9 +27,10 @@ __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const Ro
     bool bad = res.bad;
     if (task.mode == MODE_TOPN_LSE) {
         if (!bad && isfinite(res.m)) {
-            const float lns = logf(res.s);
+            const float lns = logf(wc ? wc->P : res.s);
             L = res.m / task.T + lns;
             U = (z - res.m) / task.T - lns;
+            if (wc && lane >= wc->cut) U = NEG_INF;
         } else {
             bad = true;
         }
@@ -73,7 +78,9 @@ __device__ __forceinline__ void finalize_shard(const RowResult<R> &res, const Ro
                                                const ShardOut &so, int lane) {
     const float top = __shfl_sync(FULL, key_val(res.list.k[0]), 0);
     const float m = task.mode == MODE_TOPN_LSE ? res.m : top;
-    const bool bad = res.bad || task.mode == MODE_SKIP || task.mode == MODE_ARGMAX || m != m || m == INFINITY;
+    // a wide row's filter needs the whole row: not a partial's job
+    const bool bad = res.bad || task.mode == MODE_SKIP || task.mode == MODE_ARGMAX || task.wide || m != m ||
+                     m == INFINITY;
 #pragma unroll
     for (int r = 0; r < DFLASH2_SHARD_LIST / 32; ++r) {
         const int p = r * 32 + lane;
@@ -126,7 +133,7 @@ __global__ void __launch_bounds__(256) k_topk16_merge(int S, int64_t rows, const
         if (m2 != m2) res.bad = true;
         else lse_combine(res.m, res.s, m2, s2, c);
     }
-    if (task.mode == MODE_SKIP || task.mode == MODE_ARGMAX) {
+    if (task.mode == MODE_SKIP || task.mode == MODE_ARGMAX || task.wide) {
         if (lane < NC) {
             cand_idx[row * NC + lane] = -1;
             cand_U[row * NC + lane] = NAN;
@@ -299,10 +306,22 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
         }
         if (done) {
             if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
-            if (so.part_idx)
+            if (so.part_idx) {
                 finalize_shard<R>(res, task, row, so, lane);
-            else
+            } else if (task.wide) {
+                // a filter that may reach past the 64 best: passes over the row
+                WideCut wc;
+                wc.cut = 0;
+                wc.P = NAN;
+                if constexpr (R == 2) {
+                    if (!res.bad && isfinite(res.m))
+                        wc = wide_cut<BF16>(sm, g, row, res.list, res.m, res.s, LOG2E / task.T, task.ek, task.top_p,
+                                            lane);
+                }
+                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane, &wc);
+            } else {
                 finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
+            }
         }
     }
 }

@@ -124,12 +124,54 @@ def test_bad_rows_and_params(ref):
     assert np.all(idx[4:] == -1) and np.all(np.isnan(U[4:]))
 
 
-def test_unsupported_params_flagged(ref):
+def wide_compare(ref, z, params, rpp, what):
+    """Rows whose filter reaches past their 64 best (top_k > 64, or top_p with top_k off).  Ids are
+    bit for bit.  A row whose kept prefix covers all 16 candidates has U and lse within 1e-4 rel
+    whatever its exact cut: moving a deep cut by a few tokens of mass ~1e-5 changes U by less.  A
+    row cut within its 16 candidates follows the near-tie rules of tests/_parity.py, bounded."""
     dev = cuda_or_skip()
-    z = torch.randn(3, 500).to(dev)
-    for k, p in [(0, 0.9), (65, 1.0), (100, 0.5)]:
-        idx, U, lse = d2.topk16(z, params=d2.sampling_params([1.0] * 3, [k] * 3, [p] * 3, device=dev))
-        assert torch.all(idx == -1) and torch.all(torch.isnan(U))
+    pg = d2.sampling_params(params["temperature"], params["top_k"], params["top_p"], device=dev)
+    idx, U, lse = (t.cpu().numpy() for t in d2.topk16(padded(z.to(dev)), params=pg, rows_per_param=rpp))
+    zc = z.cpu()
+    r_idx, r_U, r_lse, r_mg = ref.topk16(zc, params=params, rows_per_param=rpp)
+    np.testing.assert_array_equal(idx, r_idx, err_msg=what + " ids")
+    deep = np.all(np.isfinite(r_U), axis=1)
+    assert_close(U[deep], r_U[deep], what=what + " U (deep cuts)")
+    assert_close(lse[deep], r_lse[deep], what=what + " lse (deep cuts)")
+    sh = ~deep
+    if sh.any():
+        ex = _parity.Excused()
+        prow = np.repeat(params, rpp)[: z.shape[0]]
+        _parity.topk_compare(zc[sh], prow[sh], idx[sh], U[sh], lse[sh], r_idx[sh], r_U[sh], r_lse[sh], r_mg[sh], ex,
+                             what=what + " (cuts within the candidates)")
+        ex.check_bound(what=what)
+    return deep
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_wide_filters(ref, dtype):
+    """top_p with top_k off, top_k above 64 with and without top_p, on flat rows (deep cuts, found by
+    passes over the row) and peaked rows (cuts within the 64 best, no pass), V = 40000."""
+    g = torch.Generator().manual_seed(21)
+    rows_per = 3
+    flat = torch.randn(8 * rows_per, 40000, generator=g) * 1.5
+    peaked = synth.spike_logits(8 * rows_per, 40000, torch.Generator().manual_seed(22), "cpu")
+    z = torch.cat([flat, peaked]).to(dtype)
+    T = [1.0, 0.7, 1.2, 1.0, 0.9, 1.0, 2.0, 1.0] * 2
+    k = [0, 200, 1000, 0, 65, 30000, 0, 100] * 2
+    p = [0.9, 1.0, 0.8, 0.5, 0.95, 0.99, 0.3, 1.0] * 2
+    deep = wide_compare(ref, z, synth.make_params(16, T, k, p), rows_per, f"wide {dtype}")
+    assert deep.any() and (~deep).any()
+
+
+def test_wide_full_size(ref):
+    """The 27B drafter's rows (448 x 151936 bf16) with top_p 0.95 and top_k off: every row."""
+    dev = cuda_or_skip()
+    shp = synth.WORKLOADS["27b_sampled"]
+    g = torch.Generator(device=dev).manual_seed(shp.seed)
+    z = synth.spike_logits(shp.B * shp.K, shp.V, g, dev).to(shp.dtype)
+    wide_compare(ref, z.cpu(), synth.make_params(shp.B, 1.0, 0, 0.95), shp.K, "27b top_p 0.95")
+    assert d2.device_error() == 0
 
 
 def test_empty_and_invalid(ref):
