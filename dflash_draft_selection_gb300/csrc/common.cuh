@@ -345,27 +345,22 @@ __device__ __forceinline__ RowTask decode_row(const dflash2_sampling *P, int64_t
     t.T = T;
     t.top_p = tp;
     if (!filtered) {
-        if (target) {
-            t.mode = MODE_SKIP;
-            t.nsel = 0;
-            t.status = DFLASH2_ST_UNSUPPORTED;
+        t.mode = MODE_TOPN_LSE;
+        if (target) {  // the whole row is p's support: the 64 best, the log normaliser, then passes
+            t.nsel = DFLASH2_MAX_TOPK;
+            t.ek = static_cast<int>(V);
+            t.wide = true;
         } else {
-            t.mode = MODE_TOPN_LSE;
             t.nsel = NC;
         }
         return t;
     }
     if (ek > DFLASH2_MAX_TOPK) {
-        if (!target) {  // draft: the 64 best and the log normaliser; the cut may need further passes
-            t.mode = MODE_TOPN_LSE;
-            t.nsel = DFLASH2_MAX_TOPK;
-            t.ek = static_cast<int>(ek);
-            t.wide = true;
-            return t;
-        }
-        t.mode = MODE_SKIP;
-        t.nsel = 0;
-        t.status = DFLASH2_ST_UNSUPPORTED;
+        // the 64 best and the log normaliser; the cut may need passes over the row
+        t.mode = MODE_TOPN_LSE;
+        t.nsel = DFLASH2_MAX_TOPK;
+        t.ek = static_cast<int>(ek);
+        t.wide = true;
         return t;
     }
     t.ek = static_cast<int>(ek);

@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
                 if constexpr (R == 2) {
                     if (!res.bad && isfinite(res.m))
                         wc = wide_cut<BF16>(sm, g, row, res.list, res.m, res.s, LOG2E / task.T, task.ek, task.top_p,
-                                            lane);
+                                            false, lane);
                 }
                 finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane, &wc);
             } else {

@@ -21,6 +21,7 @@
 #include "filter.cuh"
 #include "host.hpp"
 #include "rowscan.cuh"
+#include "wide.cuh"
 
 namespace dfl {
 
@@ -109,6 +110,8 @@ struct DrawScratch {
     int32_t ids[DFLASH2_MAX_TOPK];
     int32_t sid[DFLASH2_MAX_TOPK];
     float sw[DFLASH2_MAX_TOPK];
+    double wr[NC];      // wide rows' draws: each candidate's r
+    int32_t wcand[NC];  // and its id
 };
 static_assert(sizeof(DrawScratch) <= sizeof(ScanSmem::scratch), "the draw scratch fits the completion warp's scratch");
 
@@ -286,6 +289,219 @@ __device__ void accept_request(const VerifyArgs &a, const dflash2_sampling *para
     }
 }
 
+// ------------------------------------------------------ wide target rows --
+// A sampled target row whose p reaches past its 64 best (top_p with top_k
+// off, top_k above 64, or no filter at all): p(v) = e^((z_v - m)/T) / P on
+// the tokens whose order key reaches key_cut (all of them when key_cut is 0),
+// 0 elsewhere.
+
+// p of token v of the row (0 outside the kept set or the vocabulary).
+template <bool BF16>
+__device__ __forceinline__ double wide_p(const char *rowp, int64_t V, int32_t v, const WideCut &wc, float m, float c) {
+    if (v < 0 || v >= V) return 0.0;
+    const float z = VecLoad<BF16>::scalar(rowp, v);
+    if (!(make_key(z, static_cast<uint32_t>(v)) >= wc.key_cut)) return 0.0;
+    return static_cast<double>(ex2((z - m) * c)) / static_cast<double>(wc.P);
+}
+
+// r(v) of the draw: p(v) on the kept set, with the candidates' r in place
+// of their p (sc.wcand / sc.wr, when use_cand).  Per element, any lane.
+__device__ __forceinline__ double wide_r(float z, uint32_t v, const WideCut &wc, float m, float c,
+                                         const DrawScratch &sc, bool use_cand) {
+    double r = make_key(z, v) >= wc.key_cut ? static_cast<double>(ex2((z - m) * c)) / static_cast<double>(wc.P) : 0.0;
+    if (use_cand) {
+#pragma unroll 4
+        for (int j = 0; j < NC; ++j)
+            if (static_cast<int32_t>(v) == sc.wcand[j]) r = sc.wr[j];
+    }
+    return r;
+}
+
+// Inverse CDF over ascending token ids of r (the residual max(0, p - q) with
+// the candidates' q, or p itself for the bonus and when the residual has no
+// mass): the first token whose running weight exceeds u * Z; if rounding
+// leaves none, the last token with a positive weight.  One pass of block sums
+// (blocks of at most 256 per row, in shared memory), then the crossing block
+// element by element.  Warp-uniform.
+template <bool BF16>
+__device__ int32_t wide_draw(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, int64_t row, const WideCut &wc, float m,
+                             float c, int32_t cand, float qv, bool has_q, float u, int lane) {
+    using VL = VecLoad<BF16>;
+    constexpr int VE = VL::VE;
+    const char *rowp = g.base + row * g.ld_bytes;
+    const int64_t V = g.V;
+    // the candidates' p and r, and the residual's total Z = 1 - sum_j min(p_j, q_j)
+    const double pj = has_q && lane < NC ? wide_p<BF16>(rowp, V, cand, wc, m, c) : 0.0;
+    double rj = has_q && lane < NC ? (pj > qv ? pj - qv : 0.0) : 0.0;
+    double mn = has_q && lane < NC ? (pj < qv ? pj : static_cast<double>(qv)) : 0.0;
+#pragma unroll
+    for (int d = 16; d >= 1; d >>= 1) mn += __shfl_xor_sync(FULL, mn, d);
+    double Z = has_q ? 1.0 - mn : 1.0;
+    bool use_cand = has_q;
+    if (!(Z > 1e-12)) {  // no residual mass: draw from p
+        Z = 1.0;
+        use_cand = false;
+    }
+    if (lane < NC) {
+        sc.wcand[lane] = use_cand ? cand : -1;
+        sc.wr[lane] = rj;
+    }
+    __syncwarp();
+    const double thr = static_cast<double>(u) * Z;
+    // block sums
+    int64_t blk = (V + 255) / 256;
+    blk = (blk + 32 * VE - 1) / (32 * VE) * (32 * VE);  // whole vectors for every lane
+    const int nblk = static_cast<int>((V + blk - 1) / blk);
+    for (int bi = 0; bi < nblk; ++bi) {
+        const int64_t b0 = bi * blk, b1 = (b0 + blk < V ? b0 + blk : V);
+        double acc = 0.0;
+        for (int64_t e0 = b0 + lane * VE; e0 < b1; e0 += 32 * VE) {
+            float x[VE];
+            if (e0 + VE <= b1 && e0 + VE <= (V * (BF16 ? 2 : 4)) / 16 * (16 / (BF16 ? 2 : 4))) {
+                VL::unpack(__ldcs(reinterpret_cast<const uint4 *>(rowp + e0 * (BF16 ? 2 : 4))), x);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VE; ++e) x[e] = e0 + e < b1 ? VL::scalar(rowp, e0 + e) : NEG_INF;
+            }
+#pragma unroll
+            for (int e = 0; e < VE; ++e)
+                if (e0 + e < b1 && make_key(x[e], static_cast<uint32_t>(e0 + e)) >= wc.key_cut)
+                    acc += static_cast<double>(ex2((x[e] - m) * c));
+        }
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(FULL, acc, d);
+        acc /= static_cast<double>(wc.P);
+        // the candidates of this block count with their r instead of their p
+        double corr = use_cand && lane < NC && cand >= b0 && cand < b1 ? pj - rj : 0.0;
+#pragma unroll
+        for (int d = 16; d >= 1; d >>= 1) corr += __shfl_xor_sync(FULL, corr, d);
+        if (lane == 0) sm.wide.mass[bi] = acc - corr;
+    }
+    __syncwarp();
+    // the crossing block: lane l holds blocks 8l .. 8l + 7
+    double loc[8], ls = 0.0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int bi = lane * 8 + i;
+        loc[i] = bi < nblk ? sm.wide.mass[bi] : 0.0;
+        ls += loc[i];
+    }
+    double before = ls;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const double t = __shfl_up_sync(FULL, before, d);
+        if (lane >= d) before += t;
+    }
+    before -= ls;
+    int hitb = -1, lastb = -1;
+    double cb = before;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        if (loc[i] > 0.0) {
+            if (hitb < 0 && cb + loc[i] > thr) hitb = lane * 8 + i;
+            lastb = lane * 8 + i;
+        }
+        if (hitb < 0) cb += loc[i];
+    }
+    const uint32_t hm = __ballot_sync(FULL, hitb >= 0);
+    const uint32_t lm = __ballot_sync(FULL, lastb >= 0);
+    if (!hm && !lm) return -1;
+    const bool fallback = hm == 0;
+    const int src = fallback ? 31 - __clz(lm) : __ffs(hm) - 1;
+    const int B = __shfl_sync(FULL, fallback ? lastb : hitb, src);
+    double cum0 = __shfl_sync(FULL, cb, src);  // running weight before block B
+    if (fallback) cum0 = -1.0;
+    // within block B: lane l takes elements b0 + l * per .. + per - 1 in order
+    const int64_t b0 = B * blk, b1 = (b0 + blk < V ? b0 + blk : V);
+    const int64_t per = blk / 32;
+    double sub = 0.0;
+    int64_t lastpos = -1;
+    for (int64_t e = b0 + lane * per; e < b0 + (lane + 1) * per && e < b1; ++e) {
+        const double r = wide_r(VL::scalar(rowp, e), static_cast<uint32_t>(e), wc, m, c, sc, use_cand);
+        sub += r;
+        if (r > 0.0) lastpos = e;
+    }
+    double sb = sub;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const double t = __shfl_up_sync(FULL, sb, d);
+        if (lane >= d) sb += t;
+    }
+    sb -= sub;
+    int32_t pick = -1;
+    if (fallback) {
+        const uint32_t pm = __ballot_sync(FULL, lastpos >= 0);
+        pick = pm ? static_cast<int32_t>(__shfl_sync(FULL, lastpos, 31 - __clz(pm))) : -1;
+        return pick;
+    }
+    const bool crosses = cum0 + sb + sub > thr && sub > 0.0;
+    const uint32_t cm = __ballot_sync(FULL, crosses);
+    if (!cm) {  // rounding: the block's last positive token
+        const uint32_t pm = __ballot_sync(FULL, lastpos >= 0);
+        return pm ? static_cast<int32_t>(__shfl_sync(FULL, lastpos, 31 - __clz(pm))) : -1;
+    }
+    const int L = __ffs(cm) - 1;
+    // lane L walks its elements in order
+    if (lane == L) {
+        double run = cum0 + sb;
+        const int64_t s1 = (b0 + (L + 1) * per < b1 ? b0 + (L + 1) * per : b1);
+        for (int64_t e = b0 + L * per; e < s1; ++e) {
+            const double r = wide_r(VL::scalar(rowp, e), static_cast<uint32_t>(e), wc, m, c, sc, use_cand);
+            if (r > 0.0) {
+                run += r;
+                if (run > thr) {
+                    pick = static_cast<int32_t>(e);
+                    break;
+                }
+            }
+        }
+        if (pick < 0) pick = static_cast<int32_t>(lastpos);  // rounding: the lane's last positive token
+    }
+    pick = __shfl_sync(FULL, pick, L);
+    __syncwarp();
+    return pick;
+}
+
+// A wide sampled row's decisions at position t of request b (as row_decide
+// takes them for rows whose p lies in their 64 best).  Warp-uniform.
+template <bool BF16>
+__device__ void row_decide_wide(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, const VerifyArgs &a, int64_t row,
+                                int64_t b, int t, const WideCut &wc, float m, float c, TRec *rec, int lane) {
+    const int K = a.K;
+    const char *rowp = g.base + row * g.ld_bytes;
+    int32_t qflag = DFLASH2_ST_OK, accepted = 0, emit = -1;
+    if (t < K) {
+        const int64_t o = (b * K + t) * NC;
+        const float qv = lane < NC ? a.q_sel[o + lane] : 0.0f;
+        const int32_t cand = lane < NC ? a.cand_idx[o + lane] : -1;
+        const int js = a.path_slot[b * K + t];
+        const int32_t d = a.path_tok[b * K + t];
+        if (__any_sync(FULL, lane < NC && (!isfinite(qv) || qv < 0.0f))) {
+            qflag = DFLASH2_ST_NAN;
+        } else {
+            const float s = warp_sum(qv);
+            if (!(a.flags & DFLASH2_VERIFY_TRUST_Q) && fabsf(s - 1.0f) > 1e-3f)
+                qflag = DFLASH2_ST_BAD_Q;
+            else if (js < 0 || js >= NC || a.cand_idx[o + js] != d)
+                qflag = DFLASH2_ST_BAD_Q;
+        }
+        if (qflag == DFLASH2_ST_OK) {
+            const float pd = static_cast<float>(wide_p<BF16>(rowp, g.V, d, wc, m, c));
+            const float qd = a.q_sel[o + js];
+            accepted = a.u_acc[b * K + t] * qd < pd ? 1 : 0;
+            if (!accepted)
+                emit = wide_draw<BF16>(sm, sc, g, row, wc, m, c, cand, qv, true, a.u_res[b * (K + 1) + t], lane);
+        }
+    } else {
+        emit = wide_draw<BF16>(sm, sc, g, row, wc, m, c, -1, 0.0f, false, a.u_res[b * (K + 1) + K], lane);
+    }
+    if (lane == 0) {
+        rec->qflag = qflag;
+        rec->accepted = accepted;
+        rec->emit = emit;
+    }
+}
+
 // Publish the row's record and, if it was the request's last row, run the
 // accept walk.  Consumer warp 0.
 template <bool SAMPLED>
@@ -336,6 +552,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()
                 scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_verify);
             else if (task.mode == MODE_TOPN)
                 scan_row<R, MODE_TOPN, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_verify);
+            else if (task.mode == MODE_TOPN_LSE)
+                scan_row<R, MODE_TOPN_LSE, BF16>(sm, g, ws, task, row, rrel, expect, w0, false, &g_err_verify);
             else
                 scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, expect, w0, true, &g_err_verify);
         }
@@ -357,6 +575,28 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()
             take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
             done = join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
             if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
+        } else if (task.mode == MODE_TOPN_LSE) {  // a wide row: the 64 best and the log normaliser
+            const float cw = LOG2E / task.T;
+            take_row<R, MODE_TOPN_LSE, BF16>(sm, g, row, res, rrel, cw, task.nsel, tail, aborted, lane, &g_err_verify);
+            done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, cw, lane);
+            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
+            if (done) {
+                const bool bad = res.bad || !isfinite(res.m);
+                if (lane == 0) {
+                    rec->n = 0;
+                    rec->flags = bad ? DFLASH2_ST_NAN : DFLASH2_ST_OK;
+                }
+                if constexpr (R == 2) {
+                    if (!bad) {
+                        const WideCut wc = wide_cut<BF16>(sm, g, row, res.list, res.m, res.s, cw, task.ek, task.top_p,
+                                                          true, lane);
+                        row_decide_wide<BF16>(sm, sc, g, a, row, row / (a.K + 1), static_cast<int>(row % (a.K + 1)),
+                                              wc, res.m, cw, rec, lane);
+                    }
+                }
+                row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
+            }
+            continue;
         } else {
             take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
             if (blockIdx.x == range_owner(g, row * g.cpr)) {

@@ -19,6 +19,7 @@ namespace dfl {
 struct WideCut {
     int64_t cut;
     float P;
+    uint64_t key_cut;  // the order key of the last kept token (make_key); 0: every token is kept
 };
 
 __device__ __forceinline__ uint32_t wide_key(float x) { return f2ord(x == 0.0f ? 0.0f : x); }
@@ -65,6 +66,50 @@ __device__ void wide_hist(const ScanGeom &g, int64_t row, uint32_t prefix, int s
         }
     }
     for (int64_t i = nvec * VE + lane; i < g.V; i += 32) take(VL::scalar(rowp, i));  // the ragged end
+    __syncwarp();
+}
+
+// Histogram of bits [shift, shift + 8) of ~id for the elements of `row`
+// whose ordered value key is vkey and whose ~id bits above shift + 8 equal
+// `prefix`: a select over ~id finds ties in increasing id.  Counts only.
+template <bool BF16>
+__device__ void wide_hist_id(const ScanGeom &g, int64_t row, uint32_t vkey, uint32_t prefix, int shift,
+                             ScanSmem::WideHist &h, int lane) {
+    using VL = VecLoad<BF16>;
+    constexpr int VE = VL::VE;
+    constexpr int esz = BF16 ? 2 : 4;
+    for (int i = lane; i < 256; i += 32) {
+        h.cnt[i] = 0;
+        h.mass[i] = 0.0;
+    }
+    __syncwarp();
+    const char *rowp = g.base + row * g.ld_bytes;
+    const int64_t nvec = g.V * esz / 16;
+    auto take = [&](float x, uint32_t id) {
+        if (wide_key(x) != vkey) return;
+        const uint32_t k = ~id;
+        if (shift < 24 && (k >> (shift + 8)) != prefix) return;
+        atomicAdd(&h.cnt[(k >> shift) & 255u], 1u);
+    };
+#pragma unroll 1
+    for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t vi = v0 + u * 32;
+            v[u] = vi < nvec ? __ldcs(reinterpret_cast<const uint4 *>(rowp) + vi)
+                             : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (v0 + u * 32 >= nvec) continue;
+            float x[VE];
+            VL::unpack(v[u], x);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) take(x[e], static_cast<uint32_t>((v0 + u * 32) * VE + e));
+        }
+    }
+    for (int64_t i = nvec * VE + lane; i < g.V; i += 32) take(VL::scalar(rowp, i), static_cast<uint32_t>(i));
     __syncwarp();
 }
 
@@ -186,14 +231,46 @@ __device__ uint32_t wide_select(ScanSmem &sm, const ScanGeom &g, int64_t row, fl
     return prefix << (32 - 8 * levels);
 }
 
+// The id of the n-th (from 1) lowest-id element whose ordered value key is
+// vkey: a count select over ~id, four passes.  Warp-uniform.
+template <bool BF16>
+__device__ uint32_t wide_tie_id(ScanSmem &sm, const ScanGeom &g, int64_t row, uint32_t vkey, int64_t n, int lane) {
+    uint32_t prefix = 0;
+    int64_t ca = 0;
+    for (int L = 0; L < 4; ++L) {
+        const int shift = 24 - 8 * L;
+        wide_hist_id<BF16>(g, row, vkey, prefix, shift, sm.wide, lane);
+        int64_t ac;
+        double am;
+        const int bin = wide_pick(sm.wide, false, 0.0, n - ca, &ac, &am, lane);
+        ca += ac;
+        prefix = (prefix << 8) | static_cast<uint32_t>(bin);
+    }
+    return ~prefix;
+}
+
+// The order key of the last kept token when the cut keeps n_t of the ties
+// at ordered value key vkey (ties kept lowest id first).
+template <bool BF16>
+__device__ uint64_t wide_boundary(ScanSmem &sm, const ScanGeom &g, int64_t row, uint32_t vkey, int64_t n_t,
+                                  unsigned int ties, int lane) {
+    if (n_t >= static_cast<int64_t>(ties)) return static_cast<uint64_t>(vkey) << 32;  // every tie kept
+    const uint32_t id = wide_tie_id<BF16>(sm, g, row, vkey, n_t, lane);
+    return (static_cast<uint64_t>(vkey) << 32) | static_cast<uint32_t>(~id);
+}
+
 // The wide filter's cut for a row with maximum m (raw), total mass S_all
 // relative to it, top_k = ek (<= V; > 64) and top_p = tp, given its 64 best
 // keys in `list` (R = 2).  Warp-uniform; the completion warp only.
 template <bool BF16>
 __device__ WideCut wide_cut(ScanSmem &sm, const ScanGeom &g, int64_t row, const WarpList<2> &list, float m,
-                            float S_all, float c, int64_t ek, float tp, int lane) {
+                            float S_all, float c, int64_t ek, float tp, bool want_key, int lane) {
     WideCut w;
+    w.key_cut = 0;
+    w.cut = g.V;
+    w.P = S_all;
     const bool top_k = ek < g.V;
+    if (!top_k && !(tp < 1.0f)) return w;  // no filter: the whole row
     if (!top_k) {
         // top_p alone: does the cut fall within the 64 best?
         float e[2];
@@ -215,6 +292,7 @@ __device__ WideCut wide_cut(ScanSmem &sm, const ScanGeom &g, int64_t row, const 
                 const int j = __ffs(hit) - 1;
                 w.cut = r * 32 + j + 1;
                 w.P = __shfl_sync(FULL, cum, j);
+                w.key_cut = list.at(static_cast<int>(w.cut) - 1);
                 return w;
             }
             base = __shfl_sync(FULL, cum, 31);
@@ -233,6 +311,7 @@ __device__ WideCut wide_cut(ScanSmem &sm, const ScanGeom &g, int64_t row, const 
         S_k = ma + static_cast<double>(n_tk) * ex2((ord2f(key_k) - m) * c);
         w.cut = ek;
         w.P = static_cast<float>(S_k);
+        if (want_key && !(tp < 1.0f)) w.key_cut = wide_boundary<BF16>(sm, g, row, key_k, n_tk, ties, lane);
     }
     if (tp < 1.0f) {
         // top_k off: the threshold is top_p of the whole row's mass, summed in fp64 by the select's
@@ -251,8 +330,16 @@ __device__ WideCut wide_cut(ScanSmem &sm, const ScanGeom &g, int64_t row, const 
             if (top_k && key_p == key_k && n_tp > n_tk) n_tp = n_tk;
             w.cut = ca + n_tp;
             w.P = static_cast<float>(ma + static_cast<double>(n_tp) * wp);
+            if (want_key) w.key_cut = wide_boundary<BF16>(sm, g, row, key_p, n_tp, ties, lane);
+        } else if (want_key) {
+            // rounding put the top_p cut below the top_k-th token: keep the top_k cut
+            unsigned int tk_ties = 0;
+            int64_t ca2;
+            double ma2, unused;
+            const uint32_t kk = wide_select<BF16>(sm, g, row, m, c, false, 0.0, 0.0, ek, &ca2, &ma2, &tk_ties, &unused,
+                                                  lane);
+            w.key_cut = wide_boundary<BF16>(sm, g, row, kk, ek - ca2, tk_ties, lane);
         }
-        // else rounding put the top_p cut below the top_k-th token: keep the top_k cut
     }
     return w;
 }

@@ -105,8 +105,11 @@ typedef struct {
  *          filter drops.
  * lse      [rows] f32: the log normaliser on the z / T' scale (T' = 1 for
  *          greedy rows), so that kept candidates have U = z / T' - lse.
- * A row holding a NaN or +Inf, or nothing above -Inf, or with invalid or
- * unsupported parameters, gets cand_idx -1, U NaN and lse NaN.
+ * A row holding a NaN or +Inf, or nothing above -Inf, or with invalid
+ * parameters, gets cand_idx -1, U NaN and lse NaN.  Every filter is
+ * supported: a row whose kept prefix reaches past its 64 best tokens (top_k
+ * above 64, or top_p with top_k off) is finished with further passes over
+ * the row (a radix select of the cut by count and by mass).
  * ws: dflash2_topk16_workspace_bytes(rows) bytes (the kernel splits long rows
  *   over several CTAs and combines the parts there).
  * Errors: INVALID_ARG if a pointer is NULL or misaligned, rows < 0, V < 16,
@@ -166,8 +169,9 @@ dflash2_status dflash2_topk16_noalloc(const void *logits, dflash2_dtype dt, int6
  *   part_m [rows] f32: the slice's largest logit;
  *   part_s [rows] f32: the sum over the slice of exp((z - part_m) / T'), T'
  *     the temperature (1 for greedy rows); 0 for filtered rows.
- *   A row with a NaN or +Inf in the slice, or invalid or unsupported
- *   parameters, gets -1 ids and NaN m and s.  A slice of masked tokens (all
+ *   A row with a NaN or +Inf in the slice, invalid parameters, or a filter
+ *   that needs the whole row (top_k above 64, or top_p with top_k off), gets
+ *   -1 ids and NaN m and s.  A slice of masked tokens (all
  *   -inf) is not an error: m = -inf, s = 0.
  *   ws: dflash2_topk16_workspace_bytes(rows).  Errors: those of dflash2_topk16
  *   (with V_shard as V), and INVALID_ARG for id_offset < 0 or
@@ -286,7 +290,10 @@ dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand
  *   u_acc[t] * q < p at the drafted token; on a reject they draw from
  *   max(0, p - q) (normalised; from p when its total is <= 1e-12) by inverse
  *   CDF over ascending token ids with u_res[t]; after K accepts they draw the
- *   bonus token from p_K with u_res[K].
+ *   bonus token from p_K with u_res[K].  Every filter is supported: when
+ *   p's support reaches past the row's 64 best tokens (no filter, top_p with
+ *   top_k off, top_k above 64), the cut is found by further passes over the
+ *   row and the residual and bonus draws walk the whole row in token-id order.
  * Outputs: accept_len [B] in 0..K; out_tok [B, K+1]: the accepted tokens,
  *   then the corrected or bonus token, then -1; status [B] (DFLASH2_ST_*).
  *   A request with status != 0 commits nothing (accept_len 0, all -1).

@@ -111,21 +111,27 @@ def test_status_rows(ref):
     assert st2[1] == 0
 
 
-def test_unsupported_target_params():
-    dev = cuda_or_skip()
-    B, K, V = 2, 2, 256
-    y = torch.randn(B * (K + 1), V, device=dev)
-    z = torch.zeros(B, K, dtype=torch.int32, device=dev)
-    c = torch.zeros(B, K, 16, dtype=torch.int32, device=dev)
-    q = torch.full((B, K, 16), 1 / 16, device=dev)
-    u = torch.rand(B, K + 1, device=dev)
-    acc, out, st = d2.verify(y, z, c, q, z, params=d2.sampling_params([1.0, 1.0], [0, 65], [1.0, 1.0], device=dev),
-                             u_acc=u[:, :K].contiguous(), u_res=u)
-    assert st.tolist() == [d2.binding.ST_UNSUPPORTED] * 2
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("seed", [1, 2])
+def test_wide_target_rows(ref, seed, dtype):
+    """Sampled requests whose target distribution reaches past its 64 best tokens: no filter at all,
+    top_p with top_k off, top_k above 64 with and without top_p.  p, the accept tests, the residual
+    draw over the whole vocabulary in token-id order and the bonus draw against the oracle."""
+    B, K, V = 12, 5, 20000
+    shp = synth.small_shape("27b_sampled", B=B, K=K, V=V, hidden=64, seed=seed, target_noise=1.0, dtype=dtype)
+    inp = synth.make_inputs(shp, with_conv=False)
+    inp.params["temperature"] = np.resize(np.float32([1.0, 0.8, 1.2, 1.0]), B)
+    inp.params["top_k"] = np.resize(np.int32([0, 0, 100, 500]), B)
+    inp.params["top_p"] = np.resize(np.float32([1.0, 0.9, 1.0, 0.7]), B)
+    cand, pt, ps, q = oracle_walk_inputs(ref, inp, B, K)
+    acc, ex = check(ref, inp, cand, pt, ps, q, inp.params, B, K)
+    assert 0 < int(np.sum(acc)) < B * K      # both accepts and rejects were exercised
 
 
-def test_gpu_monte_carlo_marginals(ref):
-    """6M verify rows on the GPU: committed-token marginals within 5e-3 of p_t."""
+@pytest.mark.parametrize("k,p", [(20, 0.95), (0, 0.9)])
+def test_gpu_monte_carlo_marginals(ref, k, p):
+    """6M verify rows on the GPU: committed-token marginals within 5e-3 of p_t (top_k 20 with top_p
+    0.95, the pages' setting; and top_p 0.9 with top_k off, whose residual draws walk the whole row)."""
     dev = cuda_or_skip()
     B0, K, V = 4, 3, 2048
     shp = synth.small_shape("27b_sampled", B=B0, K=K, V=V, hidden=64, seed=31, target_noise=1.0)
@@ -139,7 +145,7 @@ def test_gpu_monte_carlo_marginals(ref):
     tl = inp.target_logits.view(B0, K + 1, V).repeat(REP, 1, 1).view(B * (K + 1), V).to(dev)
     cand_g = torch.as_tensor(np.tile(cand, (REP, 1, 1))).to(dev)
     q_g = torch.as_tensor(np.tile(qrow, (REP, 1, 1))).float().to(dev)
-    pg = d2.sampling_params([1.0] * B, [20] * B, [0.95] * B, device=dev)
+    pg = d2.sampling_params([1.0] * B, [k] * B, [p] * B, device=dev)
     ws = d2.Workspace.for_verify(B, K, dev)
     gen = torch.Generator(device=dev).manual_seed(5)
     counts = [np.zeros((B0, V)) for _ in range(K + 1)]
@@ -163,7 +169,7 @@ def test_gpu_monte_carlo_marginals(ref):
             counts[t] += torch.bincount(flat, minlength=B0 * V).view(B0, V).cpu().numpy()
     for t in range(K + 1):
         for b in range(B0):
-            n, ids, pr, _ = ref.target_dist(inp.target_logits[b * (K + 1) + t], 1.0, 20, 0.95)
+            n, ids, pr, _ = ref.target_dist(inp.target_logits[b * (K + 1) + t], 1.0, k, p)
             expect = np.zeros(V)
             expect[ids] = pr
             emp = counts[t][b] / counts[t][b].sum()
