@@ -350,7 +350,7 @@ def run_ours(args, rank, world, local):
         torch.distributed.destroy_process_group()
 
 
-AUX_WORKLOADS = ("27b_greedy", "27b_sampled", "stress")
+AUX_WORKLOADS = ("27b_greedy", "27b_sampled", "27b_nucleus", "stress")
 
 
 def kernel_pass(chain, stream, n):

@@ -18,6 +18,8 @@ Recipes (one per named workload; sigma is always a standard deviation):
 * ``27b_sampled`` as 27b_greedy with temperature 1, top_k 20, top_p 0.95 on
   both sides (the recommended sampling of the FreeToken DFlash 2 PR, "Speed")
   and U(0,1) uniforms for the walk, the accept test and the resample.
+* ``27b_nucleus`` as 27b_sampled with top_k off (top_p 0.95 alone): the kept
+  prefix reaches past the 64 best tokens of the rows.
 * ``stress``      B=256, K=15, V=262144, hidden=5120, bf16; logits as above,
   and in 5% of draft and target rows one extra uniform token is set equal to
   the row maximum.  Conv inputs [256, 16, 5120] with a per-request x_prev.
@@ -65,6 +67,8 @@ WORKLOADS = {
     "27b_greedy": Shape("27b_greedy", 64, 7, 151936, 5120, seed=3),
     "27b_sampled": Shape("27b_sampled", 64, 7, 151936, 5120, temperature=1.0, top_k=20,
                          top_p=0.95, seed=4),
+    "27b_nucleus": Shape("27b_nucleus", 64, 7, 151936, 5120, temperature=1.0, top_k=0,
+                         top_p=0.95, seed=6),
     "stress": Shape("stress", 256, 15, 262144, 5120, dup_frac=0.05, seed=5),
 }
 

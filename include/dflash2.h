@@ -65,24 +65,27 @@ enum {
     DFLASH2_ST_BAD_Q = 2,       /* a q row does not sum to 1 within 1e-3, or a drafted token is not
                                    the candidate at its slot */
     DFLASH2_ST_BAD_PARAMS = 3,  /* temperature < 0 or not finite, top_k < 0, top_p outside (0, 1] */
-    DFLASH2_ST_UNSUPPORTED = 4  /* see dflash2_sampling */
+    DFLASH2_ST_UNSUPPORTED = 4  /* kept for the ABI: no parameters produce it any more */
 };
 
 #define DFLASH2_NC 16        /* candidates per draft position ([P] item 1) */
 #define DFLASH2_MAX_K 15     /* drafted positions: [F] Details refuses k outside 1 .. block_size - 1; the pages
                                 set no bound on block_size, and the cap of 15 (block_size <= 16) is this
                                 library's own limit, not a number the pages print */
-#define DFLASH2_MAX_TOPK 64  /* largest top_k a filtered row may use */
+#define DFLASH2_MAX_TOPK 64  /* top_k up to this is taken from the row's best-key list in one pass;
+                                larger top_k, or top_p with top_k off, need further passes */
 
 /*
  * Sampling parameters of one request, applied to draft and target alike in
  * the order temperature -> top_k -> renormalise -> top_p -> renormalise
  * ([F] "Speed": temperature 1.0, top_p 0.95, top_k 20 on both sides).
  * temperature == 0 is greedy.  top_k == 0 (or >= V) and top_p == 1 switch the
- * filters off.  This build supports, for temperature > 0: any top_p with
- * 1 <= effective top_k <= 64, and no filter at all on the draft side; an
- * unfiltered sampled target row, or a filtered row with top_k == 0 or
- * top_k > 64, is DFLASH2_ST_UNSUPPORTED.
+ * filters off.  Every combination is supported.  With top_k <= 64 the row's
+ * best-key list settles the filter in one pass; with top_k above 64, or top_p
+ * with top_k off, the kept prefix may reach further and the cut is found by
+ * passes over the row (dflash2_topk16, dflash2_verify).  The fused LM head
+ * and the vocabulary-sharded merge take only rows settled by 16 or 64 best
+ * tokens and give the others -1 / NaN.
  */
 typedef struct {
     float temperature;

@@ -161,6 +161,18 @@ def _verify_follow(ref, tl, pt, cand, q, ps, params, ua, ur, acc, out, b, K, V, 
 
 
 # ------------------------------------------------------------------- topk16 ----
+def _close(g, r, rtol=1e-4, atol=1e-5):
+    """assert_close's rule as a predicate."""
+    g = np.asarray(g, np.float64)
+    r = np.asarray(r, np.float64)
+    if not (np.array_equal(np.isnan(g), np.isnan(r)) and np.array_equal(np.isinf(g), np.isinf(r))):
+        return False
+    fin = np.isfinite(r)
+    if not np.array_equal(g[np.isinf(g)], r[np.isinf(r)]):
+        return False
+    return bool(np.all(np.abs(g[fin] - r[fin]) <= atol + rtol * np.abs(r[fin])))
+
+
 def topk_compare(z, params_rows, idx, U, lse, r_idx, r_U, r_lse, r_mg, ex, what="topk16"):
     """Candidates bit-exact; U and lse within tolerance except on rows whose top_p
     cut is a near-tie, where the GPU may keep one candidate more or fewer: its
@@ -169,6 +181,11 @@ def topk_compare(z, params_rows, idx, U, lse, r_idx, r_U, r_lse, r_mg, ex, what=
     rows = idx.shape[0]
     ex.decisions += rows
     ok = r_mg >= MARGIN
+    # a near-tie cut whose outputs agree within the tolerance anyway is not excused (a cut deep in a
+    # flat row moves by a token of mass ~1e-5 and U by less than the tolerance)
+    for r in np.nonzero(~ok)[0]:
+        if _close(U[r], r_U[r]) and _close(lse[r:r + 1], r_lse[r:r + 1]):
+            ok[r] = True
     assert_close(U[ok], r_U[ok], what=what + " U")
     assert_close(lse[ok], r_lse[ok], what=what + " lse")
     zz = None

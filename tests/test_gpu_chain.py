@@ -90,7 +90,7 @@ def test_tiny_f32_whole_chain_matches_oracle_chain(ref):
     np.testing.assert_array_equal(res["out"].cpu().numpy(), out)
 
 
-@pytest.mark.parametrize("name", ["4b_greedy", "27b_greedy", "27b_sampled", "stress"])
+@pytest.mark.parametrize("name", ["4b_greedy", "27b_greedy", "27b_sampled", "27b_nucleus", "stress"])
 def test_workload_chain(ref, name):
     dev = cuda_or_skip()
     inp = synth.make_inputs(synth.WORKLOADS[name], device=dev, with_conv=False)
