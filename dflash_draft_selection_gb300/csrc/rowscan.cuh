@@ -60,6 +60,7 @@ constexpr int VEC_PER_CHUNK = CHUNK_BYTES / 16;
 constexpr int VEC_PER_LANE = VEC_PER_CHUNK / 32;
 constexpr int RING = 128;             // slice-key ring of a streaming warp (a power of two)
 constexpr int GCAP = 128;             // element keys the completion warp gathers at once (its scratch)
+constexpr int WIDE_QCAP = 64;        // wide rows a CTA defers to its epilogue
 constexpr int MAX_SCAN_GRID = 1024;   // CTAs of a scan launch (partial records are sized for it)
 constexpr long long WAIT_CYCLES = 4000000000ll;  // ~2 s at 2 GHz
 constexpr long long DRAIN_CYCLES = 200000000ll;  // ~0.1 s
@@ -154,9 +155,18 @@ struct ScanSmem {
         unsigned int ring_end[SCAN_WARPS];  // 1 + the warp's ring count at its end of the row; 0 before
     } hand[2];
     alignas(16) unsigned char scratch[GCAP * 8];  // the completion warp's gathered keys; verify's draws
-    struct WideHist {                             // the completion warp's histogram for wide rows
-        double mass[256];                         // fp64: a bin may sum 10^5 weights
-        unsigned int cnt[256];
+    // Wide rows (a filter that reaches past the 64 best): the passes'
+    // histogram, and the rows whose passes wait for the CTA's epilogue.
+    struct WideHist {
+        union {
+            struct {
+                unsigned int lo[256], hi[256];  // fixed-point masses as 32-bit halves
+            } fx;
+            double blk[256];                    // a draw's block masses
+        } u;
+        unsigned int cnt[256];                  // counts (a draw's ties per block)
+        int nq;                                 // rows deferred to the epilogue
+        int q[WIDE_QCAP];                       // their index relative to the CTA's first row
     } wide;
     alignas(128) unsigned char buf[SCAN_WARPS][WSTAGES][CHUNK_BYTES];
 };
@@ -1109,6 +1119,7 @@ __device__ __forceinline__ void scan_init(ScanSmem &sm) {
             mbar_init(&sm.slot_empty[s], 1);
         }
         sm.floor_ord[0] = sm.floor_ord[1] = 0;
+        sm.wide.nq = 0;
         for (int w = 0; w < SCAN_WARPS; ++w) {
             sm.ring_head[w] = sm.ring_tail[w] = 0;
             sm.hand[0].ring_end[w] = sm.hand[1].ring_end[w] = 0;

@@ -58,6 +58,37 @@ __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const Ro
     if (lane == 0) lse[row] = L;
 }
 
+// A wide row whose cut needs passes waits for the CTA's epilogue: its ids
+// go out now, its logits (in cand_U) and maximum (in lse) until then.
+template <int R>
+__device__ __forceinline__ void defer_draft(ScanSmem &sm, const RowResult<R> &res, int64_t row, int rrel,
+                                            int32_t *cand_idx, float *cand_U, float *lse, int lane) {
+    const uint64_t k = res.list.k[0];
+    if (lane < NC) {
+        cand_idx[row * NC + lane] = key_idx(k);
+        cand_U[row * NC + lane] = key_val(k);
+    }
+    const int n = sm.wide.nq;
+    __syncwarp();
+    if (lane == 0) {
+        lse[row] = res.m;
+        sm.wide.q[n] = rrel;
+        sm.wide.nq = n + 1;
+    }
+    __syncwarp();
+}
+
+// The epilogue's outputs of a deferred row (as finalize_draft writes them).
+__device__ __forceinline__ void finalize_deferred(const RowTask &task, int64_t row, float m, const WideCut &wc,
+                                                  float *cand_U, float *lse, int lane) {
+    const float lns = logf(wc.P);
+    if (lane < NC) {
+        const float z = cand_U[row * NC + lane];
+        cand_U[row * NC + lane] = lane < wc.cut ? (z - m) / task.T - lns : NEG_INF;
+    }
+    if (lane == 0) lse[row] = m / task.T + lns;
+}
+
 // Outputs of a vocabulary shard's partial (dflash2_topk16_shard); part_idx
 // NULL for the ordinary call.
 struct ShardOut {
@@ -273,55 +304,82 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
                 scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, expect, w0, true, &g_err_topk);
         }
         if (ws.aborted) stream_drain(sm, ws, w);
-        return;
-    }
-    bool aborted = false;
-    uint32_t tail[SCAN_WARPS] = {0, 0, 0, 0};  // ring keys taken, per streaming warp
-    for (int64_t row = r_first; row <= r_last; ++row) {
-        const int rrel = static_cast<int>(row - r_first);
-        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V_params, false);
-        const float c = LOG2E / task.T;
-        RowResult<R> res;
-        bool done;
-        if (!SAMPLED || task.mode == MODE_TOPN_LSE) {
-            take_row<R, MODE_TOPN_LSE, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
-            done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, c, lane);
-        } else if (task.mode == MODE_TOPN) {
-            take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
-            done = join_parts<R, MODE_TOPN>(g, sw, row, res, c, lane);
-        } else {
-            take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
-            if (blockIdx.x == range_owner(g, row * g.cpr)) {
+        if constexpr (!SAMPLED) return;  // greedy rows are never wide
+    } else {
+        bool aborted = false;
+        uint32_t tail[SCAN_WARPS] = {0, 0, 0, 0};  // ring keys taken, per streaming warp
+        for (int64_t row = r_first; row <= r_last; ++row) {
+            const int rrel = static_cast<int>(row - r_first);
+            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V_params, false);
+            const float c = LOG2E / task.T;
+            RowResult<R> res;
+            bool done;
+            if (!SAMPLED || task.mode == MODE_TOPN_LSE) {
+                take_row<R, MODE_TOPN_LSE, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
+                done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, c, lane);
+            } else if (task.mode == MODE_TOPN) {
+                take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
+                done = join_parts<R, MODE_TOPN>(g, sw, row, res, c, lane);
+            } else {
+                take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, c, task.nsel, tail, aborted, lane, &g_err_topk);
+                if (blockIdx.x == range_owner(g, row * g.cpr)) {
+                    if (so.part_idx) {
+                        finalize_shard<R>(res, task, row, so, lane);
+                    } else {
+                        if (lane < NC) {
+                            cand_idx[row * NC + lane] = -1;
+                            cand_U[row * NC + lane] = NAN;
+                        }
+                        if (lane == 0) lse[row] = NAN;
+                    }
+                }
+                continue;
+            }
+            if (done) {
+                if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
                 if (so.part_idx) {
                     finalize_shard<R>(res, task, row, so, lane);
-                } else {
-                    if (lane < NC) {
-                        cand_idx[row * NC + lane] = -1;
-                        cand_U[row * NC + lane] = NAN;
+                } else if (task.wide) {
+                    // a filter that may reach past the 64 best: the cut from the
+                    // list, else passes over the row, in the epilogue if the queue
+                    // has room
+                    WideCut wc;
+                    wc.cut = 0;
+                    wc.P = NAN;
+                    bool ready = true;
+                    if constexpr (R == 2) {
+                        const float c = LOG2E / task.T;
+                        if (!res.bad && isfinite(res.m) &&
+                            !wide_cut_list<BF16>(res.list, res.m, res.s, c, task.ek, task.top_p, g.V, &wc, lane)) {
+                            if (sm.wide.nq < WIDE_QCAP) {
+                                defer_draft<R>(sm, res, row, rrel, cand_idx, cand_U, lse, lane);
+                                ready = false;
+                            } else {
+                                wc = wide_cut_passes<BF16>(Team{lane, 32}, sm, g, row, res.m, c, task.ek, task.top_p,
+                                                           lane);
+                            }
+                        }
                     }
-                    if (lane == 0) lse[row] = NAN;
+                    if (ready) finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane, &wc);
+                } else {
+                    finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
                 }
             }
-            continue;
         }
-        if (done) {
-            if (!res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
-            if (so.part_idx) {
-                finalize_shard<R>(res, task, row, so, lane);
-            } else if (task.wide) {
-                // a filter that may reach past the 64 best: passes over the row
-                WideCut wc;
-                wc.cut = 0;
-                wc.P = NAN;
-                if constexpr (R == 2) {
-                    if (!res.bad && isfinite(res.m))
-                        wc = wide_cut<BF16>(sm, g, row, res.list, res.m, res.s, LOG2E / task.T, task.ek, task.top_p,
-                                            false, lane);
-                }
-                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane, &wc);
-            } else {
-                finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
-            }
+    }
+    if constexpr (SAMPLED) {
+        // the deferred wide rows, on all five warps
+        __syncthreads();
+        const Team tm{static_cast<int>(threadIdx.x), SCAN_THREADS};
+        const int nq = sm.wide.nq;
+        for (int i = 0; i < nq; ++i) {
+            const int64_t row = r_first + sm.wide.q[i];
+            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V_params, false);
+            const float m = lse[row];
+            const WideCut wc =
+                wide_cut_passes<BF16>(tm, sm, g, row, m, LOG2E / task.T, task.ek, task.top_p, lane);
+            if (w == 0) finalize_deferred(task, row, m, wc, cand_U, lse, lane);
+            tm.sync();
         }
     }
 }

@@ -291,48 +291,214 @@ __device__ void accept_request(const VerifyArgs &a, const dflash2_sampling *para
 
 // ------------------------------------------------------ wide target rows --
 // A sampled target row whose p reaches past its 64 best (top_p with top_k
-// off, top_k above 64, or no filter at all): p(v) = e^((z_v - m)/T) / P on
-// the tokens whose order key reaches key_cut (all of them when key_cut is 0),
-// 0 elsewhere.
+// off, top_k above 64, or no filter at all): p(v) = w_v / P on the tokens
+// the WideCut keeps, 0 elsewhere, with w_v = 2^((z_v - m) c) counted in the
+// fixed point of the filter's passes.  The residual draw is an inverse CDF
+// over ascending ids: block sums of the row (at most 255 blocks, one team
+// pass that also counts each block's ties at the cut's value, so that the
+// lowest-id ties are the kept ones), then the crossing block element by
+// element.
 
-// p of token v of the row (0 outside the kept set or the vocabulary).
-template <bool BF16>
-__device__ __forceinline__ double wide_p(const char *rowp, int64_t V, int32_t v, const WideCut &wc, float m, float c) {
-    if (v < 0 || v >= V) return 0.0;
-    const float z = VecLoad<BF16>::scalar(rowp, v);
-    if (!(make_key(z, static_cast<uint32_t>(v)) >= wc.key_cut)) return 0.0;
-    return static_cast<double>(ex2((z - m) * c)) / static_cast<double>(wc.P);
+// A wide row's state while it waits for the CTA's epilogue, kept in its
+// record's support arrays (a wide row has no listed support).
+struct WideStash {
+    float m;        // the row maximum
+    int32_t ready;  // the cut below is known (from the 64 best)
+    int32_t cut;
+    float P;
+    uint32_t vk;
+    int32_t all;
+    int32_t nkeep;
+    int32_t ties;   // -1: not known
+};
+static_assert(sizeof(WideStash) <= sizeof(int32_t) * DFLASH2_MAX_TOPK, "the stash fits a record's id array");
+
+__device__ __forceinline__ void stash_put(TRec *rec, float m, bool ready, const WideCut &wc) {
+    WideStash s;
+    s.m = m;
+    s.ready = ready ? 1 : 0;
+    s.cut = static_cast<int32_t>(wc.cut);
+    s.P = wc.P;
+    s.vk = wc.vk;
+    s.all = wc.all ? 1 : 0;
+    s.nkeep = static_cast<int32_t>(wc.nkeep);
+    s.ties = wc.ties == INT64_MAX ? -1 : static_cast<int32_t>(wc.ties);
+    *reinterpret_cast<WideStash *>(rec->ids) = s;
+}
+__device__ __forceinline__ WideStash stash_get(const TRec *rec, WideCut *wc) {
+    const WideStash s = *reinterpret_cast<const WideStash *>(rec->ids);
+    wc->cut = s.cut;
+    wc->P = s.P;
+    wc->vk = s.vk;
+    wc->all = s.all != 0;
+    wc->nkeep = s.nkeep;
+    wc->ties = s.ties < 0 ? INT64_MAX : s.ties;
+    return s;
 }
 
-// r(v) of the draw: p(v) on the kept set, with the candidates' r in place
-// of their p (sc.wcand / sc.wr, when use_cand).  Per element, any lane.
-__device__ __forceinline__ double wide_r(float z, uint32_t v, const WideCut &wc, float m, float c,
-                                         const DrawScratch &sc, bool use_cand) {
-    double r = make_key(z, v) >= wc.key_cut ? static_cast<double>(ex2((z - m) * c)) / static_cast<double>(wc.P) : 0.0;
-    if (use_cand) {
-#pragma unroll 4
-        for (int j = 0; j < NC; ++j)
-            if (static_cast<int32_t>(v) == sc.wcand[j]) r = sc.wr[j];
+// The draw's blocks: nblk <= 255 of blk elements, blk a multiple of a
+// warp's 32 vectors.
+struct WideBlocks {
+    int64_t blk;
+    int nblk;
+};
+template <bool BF16>
+__device__ __forceinline__ WideBlocks wide_blocks(int64_t V) {
+    constexpr int SEG = 32 * VecLoad<BF16>::VE;
+    int64_t blk = (V + 254) / 255;
+    blk = (blk + SEG - 1) / SEG * SEG;
+    return {blk, static_cast<int>((V + blk - 1) / blk)};
+}
+
+// One pass over the row: per block, the mass of the kept tokens relative to
+// P (h.u.blk) and the ties at the cut's value in the blocks before it
+// (h.cnt).  Team-wide; ends synchronised.
+template <bool BF16>
+__device__ void wide_block_pass(const Team &tm, ScanSmem &sm, const ScanGeom &g, int64_t row, const WideCut &wc,
+                                float m, float c, float scale, double inv, const WideBlocks &wb, int lane) {
+    using VL = VecLoad<BF16>;
+    constexpr int VE = VL::VE;
+    constexpr int esz = BF16 ? 2 : 4;
+    ScanSmem::WideHist &h = sm.wide;
+    for (int i = tm.rank; i < 256; i += tm.size) {
+        h.cnt[i] = 0;
+        h.u.fx.lo[i] = 0;
+        h.u.fx.hi[i] = 0;
     }
+    tm.sync();
+    const char *rowp = g.base + row * g.ld_bytes;
+    const int64_t nvec = g.V * esz / 16;
+    // a lane's elements: fixed-point mass above the cut's value, ties at it
+    auto tally = [&](float x, bool valid, uint64_t &q, uint32_t &t) {
+        if (!valid) return;
+        const int s = wc.all ? 1 : (wide_vk<BF16>(x) > wc.vk ? 1 : (wide_vk<BF16>(x) == wc.vk ? 2 : 0));
+        if (s == 1) q += wide_q(ex2((x - m) * c), scale);
+        if (s == 2) ++t;
+    };
+    auto publish = [&](int64_t e0, uint64_t q, uint32_t t) {  // the warp's 32 vectors lie in one block
+        const uint64_t qs = group_sum_q(FULL, q);
+        const uint32_t ts = __reduce_add_sync(FULL, t);
+        if (lane == 0 && (qs | ts)) {
+            const int bi = static_cast<int>(e0 / wb.blk);
+            fx_add(&h.u.fx.lo[bi], &h.u.fx.hi[bi], qs);
+            atomicAdd(&h.cnt[bi], ts);
+        }
+    };
+#pragma unroll 1
+    for (int64_t v0 = tm.warp() * 32; v0 < nvec; v0 += 4 * static_cast<int64_t>(tm.size)) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t vi = v0 + u * tm.size + lane;
+            v[u] = vi < nvec ? __ldcs(reinterpret_cast<const uint4 *>(rowp) + vi)
+                             : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int64_t w0 = v0 + u * tm.size;  // the warp's first vector
+            if (w0 >= nvec) break;                // warp-uniform
+            float x[VE];
+            VL::unpack(v[u], x);
+            uint64_t q = 0;
+            uint32_t t = 0;
+#pragma unroll
+            for (int e = 0; e < VE; ++e) tally(x[e], w0 + lane < nvec, q, t);
+            publish(w0 * VE, q, t);
+        }
+    }
+    if (tm.warp() == 0 && nvec * VE < g.V) {  // the ragged end (less than one vector)
+        uint64_t q = 0;
+        uint32_t t = 0;
+        const int64_t i = nvec * VE + lane;
+        tally(i < g.V ? VL::scalar(rowp, i) : NEG_INF, i < g.V, q, t);
+        publish(nvec * VE, q, t);
+    }
+    tm.sync();
+    // blocks 8 lane .. 8 lane + 7 of every warp: ties before each block, the
+    // ties each keeps (the lowest ids first), its mass
+    const uint64_t qcut = wc.all ? 0ull : wide_q(ex2((wide_vval<BF16>(wc.vk) - m) * c), scale);
+    uint32_t tb[8], own = 0;
+    double mb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int bi = lane * 8 + i;
+        tb[i] = bi < wb.nblk ? h.cnt[bi] : 0u;
+        own += tb[i];
+    }
+    uint32_t before = own;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(FULL, before, d);
+        if (lane >= d) before += t;
+    }
+    before -= own;
+    const double invP = 1.0 / static_cast<double>(wc.P);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int bi = lane * 8 + i;
+        int64_t kept = wc.nkeep - static_cast<int64_t>(before);
+        kept = kept < 0 ? 0 : (kept > tb[i] ? tb[i] : kept);
+        mb[i] = bi < wb.nblk ? static_cast<double>(fx_get(h, bi) + static_cast<uint64_t>(kept) * qcut) * inv * invP
+                             : 0.0;
+        const uint32_t t = tb[i];
+        tb[i] = before;
+        before += t;
+    }
+    tm.sync();  // every warp read the sums before they are overwritten
+    if (tm.warp() == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int bi = lane * 8 + i;
+            if (bi < wb.nblk) {
+                h.u.blk[bi] = mb[i];
+                h.cnt[bi] = tb[i];
+            }
+        }
+    }
+    tm.sync();
+}
+
+// Rank by id among the ties at the cut's value of tie v: the ties of the
+// blocks before v's, then those of v's block before v.  One thread; after
+// the block pass.
+template <bool BF16>
+__device__ int64_t wide_tie_rank(const ScanSmem::WideHist &h, const char *rowp, const WideCut &wc,
+                                 const WideBlocks &wb, int64_t v) {
+    const int64_t bi = v / wb.blk;
+    int64_t r = h.cnt[bi];
+    for (int64_t e = bi * wb.blk; e < v; ++e) r += wide_vk<BF16>(VecLoad<BF16>::scalar(rowp, e)) == wc.vk;
     return r;
+}
+
+// p(v) (0 outside the kept set or the vocabulary).  A tie at the cut's
+// value needs the block pass first.  Per thread.
+template <bool BF16>
+__device__ double wide_p(const ScanSmem::WideHist &h, const char *rowp, int64_t V, int32_t v, const WideCut &wc,
+                         float m, float c, float scale, double inv, const WideBlocks &wb) {
+    if (v < 0 || v >= V) return 0.0;
+    const float z = VecLoad<BF16>::scalar(rowp, v);
+    const int s = wide_side<BF16>(wc, z);
+    if (s == 0) return 0.0;
+    if (s == 2 && wide_tie_rank<BF16>(h, rowp, wc, wb, v) >= wc.nkeep) return 0.0;
+    return static_cast<double>(wide_q(ex2((z - m) * c), scale)) * inv / static_cast<double>(wc.P);
 }
 
 // Inverse CDF over ascending token ids of r (the residual max(0, p - q) with
 // the candidates' q, or p itself for the bonus and when the residual has no
 // mass): the first token whose running weight exceeds u * Z; if rounding
-// leaves none, the last token with a positive weight.  One pass of block sums
-// (blocks of at most 256 per row, in shared memory), then the crossing block
-// element by element.  Warp-uniform.
+// leaves none, the last token with a positive weight.  After the block
+// pass; every warp of the team computes the same token.
 template <bool BF16>
-__device__ int32_t wide_draw(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, int64_t row, const WideCut &wc, float m,
-                             float c, int32_t cand, float qv, bool has_q, float u, int lane) {
+__device__ int32_t wide_draw(const Team &tm, ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, int64_t row,
+                             const WideCut &wc, float m, float c, float scale, double inv, const WideBlocks &wb,
+                             int32_t cand, float qv, bool has_q, float u, int lane) {
     using VL = VecLoad<BF16>;
-    constexpr int VE = VL::VE;
+    const ScanSmem::WideHist &h = sm.wide;
     const char *rowp = g.base + row * g.ld_bytes;
     const int64_t V = g.V;
     // the candidates' p and r, and the residual's total Z = 1 - sum_j min(p_j, q_j)
-    const double pj = has_q && lane < NC ? wide_p<BF16>(rowp, V, cand, wc, m, c) : 0.0;
-    double rj = has_q && lane < NC ? (pj > qv ? pj - qv : 0.0) : 0.0;
+    const double pj = has_q && lane < NC ? wide_p<BF16>(h, rowp, V, cand, wc, m, c, scale, inv, wb) : 0.0;
+    const double rj = has_q && lane < NC ? (pj > qv ? pj - qv : 0.0) : 0.0;
     double mn = has_q && lane < NC ? (pj < qv ? pj : static_cast<double>(qv)) : 0.0;
 #pragma unroll
     for (int d = 16; d >= 1; d >>= 1) mn += __shfl_xor_sync(FULL, mn, d);
@@ -342,50 +508,33 @@ __device__ int32_t wide_draw(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, i
         Z = 1.0;
         use_cand = false;
     }
-    if (lane < NC) {
+    if (tm.warp() == 0 && lane < NC) {
         sc.wcand[lane] = use_cand ? cand : -1;
         sc.wr[lane] = rj;
     }
-    __syncwarp();
     const double thr = static_cast<double>(u) * Z;
-    // block sums
-    int64_t blk = (V + 255) / 256;
-    blk = (blk + 32 * VE - 1) / (32 * VE) * (32 * VE);  // whole vectors for every lane
-    const int nblk = static_cast<int>((V + blk - 1) / blk);
-    for (int bi = 0; bi < nblk; ++bi) {
-        const int64_t b0 = bi * blk, b1 = (b0 + blk < V ? b0 + blk : V);
-        double acc = 0.0;
-        for (int64_t e0 = b0 + lane * VE; e0 < b1; e0 += 32 * VE) {
-            float x[VE];
-            if (e0 + VE <= b1 && e0 + VE <= (V * (BF16 ? 2 : 4)) / 16 * (16 / (BF16 ? 2 : 4))) {
-                VL::unpack(__ldcs(reinterpret_cast<const uint4 *>(rowp + e0 * (BF16 ? 2 : 4))), x);
-            } else {
-#pragma unroll
-                for (int e = 0; e < VE; ++e) x[e] = e0 + e < b1 ? VL::scalar(rowp, e0 + e) : NEG_INF;
-            }
-#pragma unroll
-            for (int e = 0; e < VE; ++e)
-                if (e0 + e < b1 && make_key(x[e], static_cast<uint32_t>(e0 + e)) >= wc.key_cut)
-                    acc += static_cast<double>(ex2((x[e] - m) * c));
-        }
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) acc += __shfl_xor_sync(FULL, acc, d);
-        acc /= static_cast<double>(wc.P);
-        // the candidates of this block count with their r instead of their p
-        double corr = use_cand && lane < NC && cand >= b0 && cand < b1 ? pj - rj : 0.0;
-#pragma unroll
-        for (int d = 16; d >= 1; d >>= 1) corr += __shfl_xor_sync(FULL, corr, d);
-        if (lane == 0) sm.wide.mass[bi] = acc - corr;
-    }
-    __syncwarp();
-    // the crossing block: lane l holds blocks 8l .. 8l + 7
+    // lane l holds blocks 8l .. 8l + 7; a candidate's block counts its r instead of its p
     double loc[8], ls = 0.0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int bi = lane * 8 + i;
-        loc[i] = bi < nblk ? sm.wide.mass[bi] : 0.0;
-        ls += loc[i];
+        loc[i] = bi < wb.nblk ? h.u.blk[bi] : 0.0;
     }
+    if (use_cand) {
+        for (int j = 0; j < NC; ++j) {
+            const int32_t cj = __shfl_sync(FULL, cand, j);
+            const double dj = __shfl_sync(FULL, pj - rj, j);
+            if (cj >= 0 && cj < V) {
+                const int64_t bj = cj / wb.blk;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (lane * 8 + i == bj) loc[i] -= dj;
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ls += loc[i];
+    tm.sync();  // the candidates' r in shared memory
     double before = ls;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
@@ -409,17 +558,46 @@ __device__ int32_t wide_draw(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, i
     const bool fallback = hm == 0;
     const int src = fallback ? 31 - __clz(lm) : __ffs(hm) - 1;
     const int B = __shfl_sync(FULL, fallback ? lastb : hitb, src);
-    double cum0 = __shfl_sync(FULL, cb, src);  // running weight before block B
-    if (fallback) cum0 = -1.0;
+    const double cum0 = fallback ? -1.0 : __shfl_sync(FULL, cb, src);  // running weight before block B
     // within block B: lane l takes elements b0 + l * per .. + per - 1 in order
-    const int64_t b0 = B * blk, b1 = (b0 + blk < V ? b0 + blk : V);
-    const int64_t per = blk / 32;
+    const int64_t b0 = B * wb.blk, b1 = (b0 + wb.blk < V ? b0 + wb.blk : V);
+    const int64_t per = wb.blk / 32;
+    const int64_t s0 = b0 + lane * per, s1 = (s0 + per < b1 ? s0 + per : b1);
+    const bool partial = !wc.all && wc.nkeep < wc.ties;
+    // ties before this lane's elements
+    uint32_t tl = 0;
+    if (partial)
+        for (int64_t e = s0; e < s1; ++e) tl += wide_vk<BF16>(VL::scalar(rowp, e)) == wc.vk;
+    uint32_t tx = tl;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t t = __shfl_up_sync(FULL, tx, d);
+        if (lane >= d) tx += t;
+    }
+    const int64_t rank0 = static_cast<int64_t>(h.cnt[B]) + (tx - tl);
+    const double invP = 1.0 / static_cast<double>(wc.P);
+    // r of element e of this lane, given the running tie rank
+    auto r_of = [&](int64_t e, int64_t &rank) -> double {
+        const float z = VL::scalar(rowp, e);
+        int s = wc.all ? 1 : (wide_vk<BF16>(z) > wc.vk ? 1 : (wide_vk<BF16>(z) == wc.vk ? 2 : 0));
+        if (s == 2) s = (!partial || rank < wc.nkeep) ? 1 : 0, ++rank;
+        double r = s == 1 ? static_cast<double>(wide_q(ex2((z - m) * c), scale)) * inv * invP : 0.0;
+        if (use_cand) {
+#pragma unroll 4
+            for (int j = 0; j < NC; ++j)
+                if (static_cast<int32_t>(e) == sc.wcand[j]) r = sc.wr[j];
+        }
+        return r;
+    };
     double sub = 0.0;
     int64_t lastpos = -1;
-    for (int64_t e = b0 + lane * per; e < b0 + (lane + 1) * per && e < b1; ++e) {
-        const double r = wide_r(VL::scalar(rowp, e), static_cast<uint32_t>(e), wc, m, c, sc, use_cand);
-        sub += r;
-        if (r > 0.0) lastpos = e;
+    {
+        int64_t rank = rank0;
+        for (int64_t e = s0; e < s1; ++e) {
+            const double r = r_of(e, rank);
+            sub += r;
+            if (r > 0.0) lastpos = e;
+        }
     }
     double sb = sub;
 #pragma unroll
@@ -428,25 +606,20 @@ __device__ int32_t wide_draw(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, i
         if (lane >= d) sb += t;
     }
     sb -= sub;
-    int32_t pick = -1;
-    if (fallback) {
-        const uint32_t pm = __ballot_sync(FULL, lastpos >= 0);
-        pick = pm ? static_cast<int32_t>(__shfl_sync(FULL, lastpos, 31 - __clz(pm))) : -1;
-        return pick;
-    }
+    const uint32_t pm = __ballot_sync(FULL, lastpos >= 0);
+    const int32_t last_tok = pm ? static_cast<int32_t>(__shfl_sync(FULL, lastpos, 31 - __clz(pm))) : -1;
+    if (fallback) return last_tok;
     const bool crosses = cum0 + sb + sub > thr && sub > 0.0;
     const uint32_t cm = __ballot_sync(FULL, crosses);
-    if (!cm) {  // rounding: the block's last positive token
-        const uint32_t pm = __ballot_sync(FULL, lastpos >= 0);
-        return pm ? static_cast<int32_t>(__shfl_sync(FULL, lastpos, 31 - __clz(pm))) : -1;
-    }
+    if (!cm) return last_tok;  // rounding: the block's last positive token
     const int L = __ffs(cm) - 1;
     // lane L walks its elements in order
+    int32_t pick = -1;
     if (lane == L) {
         double run = cum0 + sb;
-        const int64_t s1 = (b0 + (L + 1) * per < b1 ? b0 + (L + 1) * per : b1);
-        for (int64_t e = b0 + L * per; e < s1; ++e) {
-            const double r = wide_r(VL::scalar(rowp, e), static_cast<uint32_t>(e), wc, m, c, sc, use_cand);
+        int64_t rank = rank0;
+        for (int64_t e = s0; e < s1; ++e) {
+            const double r = r_of(e, rank);
             if (r > 0.0) {
                 run += r;
                 if (run > thr) {
@@ -457,18 +630,23 @@ __device__ int32_t wide_draw(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, i
         }
         if (pick < 0) pick = static_cast<int32_t>(lastpos);  // rounding: the lane's last positive token
     }
-    pick = __shfl_sync(FULL, pick, L);
-    __syncwarp();
-    return pick;
+    return __shfl_sync(FULL, pick, L);
 }
 
 // A wide sampled row's decisions at position t of request b (as row_decide
-// takes them for rows whose p lies in their 64 best).  Warp-uniform.
+// takes them for rows whose p lies in their 64 best).  Team-wide; the
+// record is written by the team's first thread.
 template <bool BF16>
-__device__ void row_decide_wide(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, const VerifyArgs &a, int64_t row,
-                                int64_t b, int t, const WideCut &wc, float m, float c, TRec *rec, int lane) {
+__device__ __noinline__ void row_decide_wide(const Team &tm, ScanSmem &sm, DrawScratch &sc, const ScanGeom &g,
+                                const VerifyArgs &a, int64_t row, int64_t b, int t, const WideCut &wc, float m,
+                                float c, TRec *rec, int lane) {
     const int K = a.K;
     const char *rowp = g.base + row * g.ld_bytes;
+    const int fxs = wide_fxs(g.V);
+    const float scale = fx_scale(fxs);
+    const double inv = fx_inv(fxs);
+    const WideBlocks wb = wide_blocks<BF16>(g.V);
+    bool blocks = false;
     int32_t qflag = DFLASH2_ST_OK, accepted = 0, emit = -1;
     if (t < K) {
         const int64_t o = (b * K + t) * NC;
@@ -486,16 +664,25 @@ __device__ void row_decide_wide(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g
                 qflag = DFLASH2_ST_BAD_Q;
         }
         if (qflag == DFLASH2_ST_OK) {
-            const float pd = static_cast<float>(wide_p<BF16>(rowp, g.V, d, wc, m, c));
+            if (d >= 0 && d < g.V && wide_side<BF16>(wc, VecLoad<BF16>::scalar(rowp, d)) == 2) {
+                wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, scale, inv, wb, lane);  // d's rank among the ties
+                blocks = true;
+            }
+            const float pd = static_cast<float>(wide_p<BF16>(sm.wide, rowp, g.V, d, wc, m, c, scale, inv, wb));
             const float qd = a.q_sel[o + js];
             accepted = a.u_acc[b * K + t] * qd < pd ? 1 : 0;
-            if (!accepted)
-                emit = wide_draw<BF16>(sm, sc, g, row, wc, m, c, cand, qv, true, a.u_res[b * (K + 1) + t], lane);
+            if (!accepted) {
+                if (!blocks) wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, scale, inv, wb, lane);
+                emit = wide_draw<BF16>(tm, sm, sc, g, row, wc, m, c, scale, inv, wb, cand, qv, true,
+                                       a.u_res[b * (K + 1) + t], lane);
+            }
         }
     } else {
-        emit = wide_draw<BF16>(sm, sc, g, row, wc, m, c, -1, 0.0f, false, a.u_res[b * (K + 1) + K], lane);
+        wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, scale, inv, wb, lane);
+        emit = wide_draw<BF16>(tm, sm, sc, g, row, wc, m, c, scale, inv, wb, -1, 0.0f, false,
+                               a.u_res[b * (K + 1) + K], lane);
     }
-    if (lane == 0) {
+    if (tm.rank == 0) {
         rec->qflag = qflag;
         rec->accepted = accepted;
         rec->emit = emit;
@@ -558,64 +745,104 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()
                 scan_row<R, MODE_ARGMAX, BF16>(sm, g, ws, task, row, rrel, expect, w0, true, &g_err_verify);
         }
         if (ws.aborted) stream_drain(sm, ws, w);
-        return;
-    }
-    bool aborted = false;
-    uint32_t tail[SCAN_WARPS] = {0, 0, 0, 0};  // ring keys taken, per streaming warp
-    for (int64_t row = r_first; row <= r_last; ++row) {
-        const int rrel = static_cast<int>(row - r_first);
-        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
-        TRec *rec = a.recs + row;
-        RowResult<R> res;
-        bool done;
-        if (!SAMPLED || task.mode == MODE_ARGMAX) {
-            take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
-            done = join_parts<R, MODE_ARGMAX>(g, sw, row, res, LOG2E, lane);
-        } else if (task.mode == MODE_TOPN) {
-            take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
-            done = join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
-            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
-        } else if (task.mode == MODE_TOPN_LSE) {  // a wide row: the 64 best and the log normaliser
-            const float cw = LOG2E / task.T;
-            take_row<R, MODE_TOPN_LSE, BF16>(sm, g, row, res, rrel, cw, task.nsel, tail, aborted, lane, &g_err_verify);
-            done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, cw, lane);
-            if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
-            if (done) {
-                const bool bad = res.bad || !isfinite(res.m);
-                if (lane == 0) {
-                    rec->n = 0;
-                    rec->flags = bad ? DFLASH2_ST_NAN : DFLASH2_ST_OK;
-                }
-                if constexpr (R == 2) {
-                    if (!bad) {
-                        const WideCut wc = wide_cut<BF16>(sm, g, row, res.list, res.m, res.s, cw, task.ek, task.top_p,
-                                                          true, lane);
-                        row_decide_wide<BF16>(sm, sc, g, a, row, row / (a.K + 1), static_cast<int>(row % (a.K + 1)),
-                                              wc, res.m, cw, rec, lane);
+        if constexpr (!SAMPLED) return;  // greedy rows are never wide
+    } else {
+        bool aborted = false;
+        uint32_t tail[SCAN_WARPS] = {0, 0, 0, 0};  // ring keys taken, per streaming warp
+        for (int64_t row = r_first; row <= r_last; ++row) {
+            const int rrel = static_cast<int>(row - r_first);
+            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
+            TRec *rec = a.recs + row;
+            RowResult<R> res;
+            bool done;
+            if (!SAMPLED || task.mode == MODE_ARGMAX) {
+                take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
+                done = join_parts<R, MODE_ARGMAX>(g, sw, row, res, LOG2E, lane);
+            } else if (task.mode == MODE_TOPN) {
+                take_row<R, MODE_TOPN, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
+                done = join_parts<R, MODE_TOPN>(g, sw, row, res, LOG2E, lane);
+                if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
+            } else if (task.mode == MODE_TOPN_LSE) {  // a wide row: the 64 best and the log normaliser
+                const float cw = LOG2E / task.T;
+                take_row<R, MODE_TOPN_LSE, BF16>(sm, g, row, res, rrel, cw, task.nsel, tail, aborted, lane, &g_err_verify);
+                done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, cw, lane);
+                if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
+                if (done) {
+                    const bool bad = res.bad || !isfinite(res.m);
+                    if (lane == 0) {
+                        rec->n = 0;
+                        rec->flags = bad ? DFLASH2_ST_NAN : DFLASH2_ST_OK;
                     }
+                    bool decided = true;
+                    if constexpr (R == 2) {
+                        if (!bad) {
+                            // the cut from the list when it decides it; the passes and
+                            // the draws in the epilogue if the queue has room
+                            WideCut wc;
+                            const bool ready =
+                                wide_cut_list<BF16>(res.list, res.m, res.s, cw, task.ek, task.top_p, g.V, &wc, lane);
+                            const int n = sm.wide.nq;
+                            if (n < WIDE_QCAP) {
+                                __syncwarp();
+                                if (lane == 0) {
+                                    stash_put(rec, res.m, ready, wc);
+                                    sm.wide.q[n] = rrel;
+                                    sm.wide.nq = n + 1;
+                                }
+                                __syncwarp();
+                                decided = false;
+                            } else {
+                                const Team t1{lane, 32};
+                                if (!ready) wc = wide_cut_passes<BF16>(t1, sm, g, row, res.m, cw, task.ek, task.top_p, lane);
+                                row_decide_wide<BF16>(t1, sm, sc, g, a, row, row / (a.K + 1),
+                                                      static_cast<int>(row % (a.K + 1)), wc, res.m, cw, rec, lane);
+                            }
+                        }
+                    }
+                    if (decided) row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
                 }
+                continue;
+            } else {
+                take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
+                if (blockIdx.x == range_owner(g, row * g.cpr)) {
+                    if (lane == 0) {
+                        rec->n = 0;
+                        rec->flags = task.status;
+                    }
+                    row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
+                }
+                continue;
+            }
+            if (done) {
+                int32_t id[2];
+                float pr[2];
+                int rn;
+                const int32_t fl = finalize_target<R>(res, task, rec, lane, id, pr, &rn);
+                if (SAMPLED && task.mode == MODE_TOPN && fl == DFLASH2_ST_OK)
+                    row_decide(a, row / (a.K + 1), static_cast<int>(row % (a.K + 1)), id, pr, rn, rec, sc, lane);
                 row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
             }
-            continue;
-        } else {
-            take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
-            if (blockIdx.x == range_owner(g, row * g.cpr)) {
-                if (lane == 0) {
-                    rec->n = 0;
-                    rec->flags = task.status;
-                }
-                row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
-            }
-            continue;
         }
-        if (done) {
-            int32_t id[2];
-            float pr[2];
-            int rn;
-            const int32_t fl = finalize_target<R>(res, task, rec, lane, id, pr, &rn);
-            if (SAMPLED && task.mode == MODE_TOPN && fl == DFLASH2_ST_OK)
-                row_decide(a, row / (a.K + 1), static_cast<int>(row % (a.K + 1)), id, pr, rn, rec, sc, lane);
-            row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
+    }
+    if constexpr (SAMPLED) {
+        // the deferred wide rows, on all five warps; the completion warp
+        // then publishes each row's record
+        __syncthreads();
+        const Team tm{static_cast<int>(threadIdx.x), SCAN_THREADS};
+        const int nq = sm.wide.nq;
+        for (int i = 0; i < nq; ++i) {
+            const int64_t row = r_first + sm.wide.q[i];
+            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
+            const float cw = LOG2E / task.T;
+            TRec *rec = a.recs + row;
+            WideCut wc;
+            const WideStash st = stash_get(rec, &wc);
+            if (!st.ready) wc = wide_cut_passes<BF16>(tm, sm, g, row, st.m, cw, task.ek, task.top_p, lane);
+            row_decide_wide<BF16>(tm, sm, sc, g, a, row, row / (a.K + 1), static_cast<int>(row % (a.K + 1)), wc,
+                                  st.m, cw, rec, lane);
+            tm.sync();
+            if (w == SCAN_WARPS) row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
+            tm.sync();
         }
     }
 }

@@ -1,347 +1,409 @@
 // wide.cuh -- rows whose sampling filter reaches past their 64 best tokens:
-// a draft row with top_k above 64, or with top_p and top_k off.  The filter
-// of the pages' sampling (temperature -> top_k -> renormalise -> top_p ->
+// a draft row with top_k above 64, or with top_p and top_k off; a sampled
+// target row whose p does the same (or has no filter at all).  The filter of
+// the pages' sampling (temperature -> top_k -> renormalise -> top_p ->
 // renormalise, FreeToken PR 857 "Speed") then keeps a prefix of the row in
 // the order key (value descending, lower id first) whose length and mass come
 // from a radix select over the ordered value bits, by count (the top_k-th
-// token) and by mass (where the cumulative mass reaches top_p), each level a
-// pass over the row by the CTA's completion warp with a 256-bin histogram of
-// counts and (fp64) masses in shared memory.  Rows whose cut lies within the 64 best
-// need no pass.
+// token) and by mass (where the running mass reaches top_p): one pass over
+// the row per 8 bits of the value, each a 256-bin histogram of counts and
+// masses in shared memory.
+//
+// The passes run on a Team: the CTA's five warps together in the scan
+// kernels' epilogue (the rows wait in a queue until the CTA streamed its
+// range), or the completion warp alone when the queue is full.
+//
+// Masses are fixed point: a weight w = 2^((z - m) c) in [0, 1] counts as
+// q = round(w 2^s) (s = 40, fewer bits for a vocabulary above 2^23), so that
+// sums of up to V of them are exact 64-bit integers whatever the order of
+// the additions.  Warp lanes that land in one bin add once (their counts and
+// masses reduced over the lanes); a 64-bit add to shared memory is two 32-bit
+// atomics with the carry taken from the low half's old value.
 #pragma once
 
 #include "rowscan.cuh"
 
 namespace dfl {
 
-// Result of the wide filter: the kept prefix has `cut` tokens and mass P,
-// relative to the row maximum m (weights 2^((z - m) c) = e^((z - m) / T)).
+// The warps that run a pass: all of the CTA's (size 160, synchronised by the
+// CTA barrier) or one (size 32).
+struct Team {
+    int rank;  // this thread's index in the team
+    int size;  // threads
+    __device__ __forceinline__ void sync() const {
+        if (size == 32)
+            __syncwarp();
+        else
+            __syncthreads();
+    }
+    __device__ __forceinline__ int warp() const { return rank >> 5; }
+    __device__ __forceinline__ int warps() const { return size >> 5; }
+};
+
+// The wide filter of a row: `cut` tokens of mass P (relative to the row
+// maximum) are kept: every token whose value key is above vk, and the nkeep
+// lowest ids of the `ties` tokens at value key vk.  all: every token kept.
 struct WideCut {
     int64_t cut;
     float P;
-    uint64_t key_cut;  // the order key of the last kept token (make_key); 0: every token is kept
+    bool all;
+    uint32_t vk;
+    int64_t nkeep;
+    int64_t ties;  // INT64_MAX when not known
 };
 
-__device__ __forceinline__ uint32_t wide_key(float x) { return f2ord(x == 0.0f ? 0.0f : x); }
-
-// Histogram (counts, masses) of bits [shift, shift + 8) of the ordered keys of
-// the elements of `row` whose key bits above shift + 8 equal `prefix` (all
-// elements when shift = 24).  Warp-uniform; the completion warp only.
+// Value keys: the order-preserving bits of the logit (-0 as +0); for bf16
+// logits the top 16 (the other 16 are the same for every bf16 of a sign).
 template <bool BF16>
-__device__ void wide_hist(const ScanGeom &g, int64_t row, uint32_t prefix, int shift, float m, float c,
-                          ScanSmem::WideHist &h, int lane) {
+__device__ __forceinline__ uint32_t wide_vk(float x) {
+    const uint32_t k = f2ord(x == 0.0f ? 0.0f : x);
+    return BF16 ? k >> 16 : k;
+}
+template <bool BF16>
+__device__ __forceinline__ float wide_vval(uint32_t vk) {
+    if (!BF16) return ord2f(vk);
+    // a bf16's ordered bits end in 16 zeros (positive) or 16 ones (negative)
+    return ord2f((vk << 16) | ((vk & 0x8000u) ? 0u : 0xffffu));
+}
+
+// Fixed-point scale: the largest s <= 40 with V 2^s < 2^63.
+__device__ __forceinline__ int wide_fxs(int64_t V) {
+    const int bits = 64 - __clzll(static_cast<unsigned long long>(V));
+    return 63 - bits < 40 ? 63 - bits : 40;
+}
+__device__ __forceinline__ float fx_scale(int s) { return __int_as_float((127 + s) << 23); }
+__device__ __forceinline__ double fx_inv(int s) { return __longlong_as_double(static_cast<long long>(1023 - s) << 52); }
+__device__ __forceinline__ uint64_t wide_q(float w, float scale) { return __float2ull_rn(w * scale); }
+
+// Sum over the lanes of `grp` of values below 2^45 (exact).
+__device__ __forceinline__ uint64_t group_sum_q(unsigned int grp, uint64_t v) {
+    const uint32_t l = __reduce_add_sync(grp, static_cast<uint32_t>(v & 0xfffffu));
+    const uint32_t h = __reduce_add_sync(grp, static_cast<uint32_t>(v >> 20));
+    return (static_cast<uint64_t>(h) << 20) + l;
+}
+__device__ __forceinline__ void fx_add(unsigned int *lo, unsigned int *hi, uint64_t v) {
+    const uint32_t a = static_cast<uint32_t>(v), b = static_cast<uint32_t>(v >> 32);
+    const uint32_t old = atomicAdd(lo, a);
+    const uint32_t carry = old + a < old ? 1u : 0u;
+    if (b + carry) atomicAdd(hi, b + carry);
+}
+__device__ __forceinline__ uint64_t fx_get(const ScanSmem::WideHist &h, int i) {
+    return (static_cast<uint64_t>(h.u.fx.hi[i]) << 32) | h.u.fx.lo[i];
+}
+__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
+    const uint32_t l = __shfl_up_sync(FULL, static_cast<uint32_t>(v), d);
+    const uint32_t h = __shfl_up_sync(FULL, static_cast<uint32_t>(v >> 32), d);
+    return (static_cast<uint64_t>(h) << 32) | l;
+}
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+    const uint32_t l = __shfl_sync(FULL, static_cast<uint32_t>(v), src);
+    const uint32_t h = __shfl_sync(FULL, static_cast<uint32_t>(v >> 32), src);
+    return (static_cast<uint64_t>(h) << 32) | l;
+}
+
+// Calls f(x, id, valid) for every element of `row`, the team's threads
+// taking 16-byte vectors in turn (four in flight per lane); whole warps
+// call f together (lanes past the row with valid false).
+template <bool BF16, typename F>
+__device__ __forceinline__ void team_for_each(const Team &tm, const ScanGeom &g, int64_t row, int lane, F &&f) {
     using VL = VecLoad<BF16>;
     constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
-    for (int i = lane; i < 256; i += 32) {
-        h.cnt[i] = 0;
-        h.mass[i] = 0.0;
-    }
-    __syncwarp();
     const char *rowp = g.base + row * g.ld_bytes;
     const int64_t nvec = g.V * esz / 16;
-    auto take = [&](float x) {
-        const uint32_t k = wide_key(x);
-        if (shift < 24 && (k >> (shift + 8)) != prefix) return;
-        const int bin = static_cast<int>((k >> shift) & 255u);
-        atomicAdd(&h.cnt[bin], 1u);
-        atomicAdd(&h.mass[bin], static_cast<double>(ex2((x - m) * c)));
-    };
 #pragma unroll 1
-    for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
+    for (int64_t v0 = tm.warp() * 32; v0 < nvec; v0 += 4 * static_cast<int64_t>(tm.size)) {
         uint4 v[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int64_t vi = v0 + u * 32;
+            const int64_t vi = v0 + u * tm.size + lane;
             v[u] = vi < nvec ? __ldcs(reinterpret_cast<const uint4 *>(rowp) + vi)
                              : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
         }
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            if (v0 + u * 32 >= nvec) continue;
+            const int64_t vi = v0 + u * tm.size + lane;
             float x[VE];
             VL::unpack(v[u], x);
 #pragma unroll
-            for (int e = 0; e < VE; ++e) take(x[e]);
+            for (int e = 0; e < VE; ++e) f(x[e], vi * VE + e, vi < nvec);
         }
     }
-    for (int64_t i = nvec * VE + lane; i < g.V; i += 32) take(VL::scalar(rowp, i));  // the ragged end
-    __syncwarp();
+    if (tm.warp() == 0) {  // the ragged end (less than one vector)
+        for (int64_t i0 = nvec * VE; i0 < g.V; i0 += 32) {
+            const int64_t i = i0 + lane;
+            f(i < g.V ? VL::scalar(rowp, i) : NEG_INF, i, i < g.V);
+        }
+    }
 }
 
-// Histogram of bits [shift, shift + 8) of ~id for the elements of `row`
-// whose ordered value key is vkey and whose ~id bits above shift + 8 equal
-// `prefix`: a select over ~id finds ties in increasing id.  Counts only.
+// Histogram of bits [shift, shift + 8) of the value keys of the elements of
+// `row` whose key bits above shift + 8 equal `prefix` (every element at the
+// top level): counts and fixed-point masses.  Team-wide; ends synchronised.
 template <bool BF16>
-__device__ void wide_hist_id(const ScanGeom &g, int64_t row, uint32_t vkey, uint32_t prefix, int shift,
-                             ScanSmem::WideHist &h, int lane) {
-    using VL = VecLoad<BF16>;
-    constexpr int VE = VL::VE;
-    constexpr int esz = BF16 ? 2 : 4;
-    for (int i = lane; i < 256; i += 32) {
+__device__ void wide_hist(const Team &tm, const ScanGeom &g, int64_t row, uint32_t prefix, int shift, float m,
+                          float c, float scale, ScanSmem::WideHist &h, int lane) {
+    constexpr int kbits = BF16 ? 16 : 32;
+    for (int i = tm.rank; i < 256; i += tm.size) {
         h.cnt[i] = 0;
-        h.mass[i] = 0.0;
+        h.u.fx.lo[i] = 0;
+        h.u.fx.hi[i] = 0;
     }
-    __syncwarp();
-    const char *rowp = g.base + row * g.ld_bytes;
-    const int64_t nvec = g.V * esz / 16;
-    auto take = [&](float x, uint32_t id) {
-        if (wide_key(x) != vkey) return;
-        const uint32_t k = ~id;
-        if (shift < 24 && (k >> (shift + 8)) != prefix) return;
-        atomicAdd(&h.cnt[(k >> shift) & 255u], 1u);
-    };
-#pragma unroll 1
-    for (int64_t v0 = lane; v0 < nvec; v0 += 32 * 4) {
-        uint4 v[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int64_t vi = v0 + u * 32;
-            v[u] = vi < nvec ? __ldcs(reinterpret_cast<const uint4 *>(rowp) + vi)
-                             : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+    tm.sync();
+    const bool top = shift + 8 >= kbits;
+    team_for_each<BF16>(tm, g, row, lane, [&](float x, int64_t, bool valid) {
+        const uint32_t k = wide_vk<BF16>(x);
+        const bool in = valid && (top || (k >> (shift + 8)) == prefix);
+        if (!__any_sync(FULL, in)) return;
+        const int bin = in ? static_cast<int>((k >> shift) & 255u) : 256;
+        const unsigned int grp = __match_any_sync(FULL, bin);
+        const uint64_t s = group_sum_q(grp, in ? wide_q(ex2((x - m) * c), scale) : 0ull);
+        if (in && lane == __ffs(grp) - 1) {
+            atomicAdd(&h.cnt[bin], static_cast<unsigned int>(__popc(grp)));
+            fx_add(&h.u.fx.lo[bin], &h.u.fx.hi[bin], s);
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (v0 + u * 32 >= nvec) continue;
-            float x[VE];
-            VL::unpack(v[u], x);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) take(x[e], static_cast<uint32_t>((v0 + u * 32) * VE + e));
-        }
-    }
-    for (int64_t i = nvec * VE + lane; i < g.V; i += 32) take(VL::scalar(rowp, i), static_cast<uint32_t>(i));
-    __syncwarp();
+    });
+    tm.sync();
 }
 
-// The bin where, from the top bin down, the running count (by_mass false)
-// or mass reaches `need`; *above_c / *above_m receive the totals of the bins
-// above it.  If rounding leaves the mass short of `need`, the lowest bin that
-// holds an element.  Warp-uniform.
-__device__ __forceinline__ int wide_pick(const ScanSmem::WideHist &h, bool by_mass, double need, int64_t need_c,
-                                         int64_t *above_c, double *above_m, int lane) {
+// The bin where, from the top bin down, the running count (by_mass false:
+// reaching need_c) or mass (qbase + the bins so far reaching need, in units
+// of 2^-s) is reached; *above_c / *above_q: the totals of the bins above it.
+// With rel_p > 0, need is first set to rel_p times qbase + the histogram's
+// whole mass (*need_io).  If the mass stays short of need, the lowest bin
+// that holds an element.  Per warp, from shared memory.
+__device__ __forceinline__ int wide_pick(const ScanSmem::WideHist &h, bool by_mass, double *need_io, double rel_p,
+                                         int64_t need_c, uint64_t qbase, double inv, int64_t *above_c,
+                                         uint64_t *above_q, int lane) {
     unsigned int c8[8];
-    double m8[8];
+    uint64_t q8[8];
     unsigned int lc = 0;
-    double lm = 0.0;
+    uint64_t lq = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int bin = 255 - (lane * 8 + i);
         c8[i] = h.cnt[bin];
-        m8[i] = h.mass[bin];
+        q8[i] = fx_get(h, bin);
         lc += c8[i];
-        lm += m8[i];
+        lq += q8[i];
     }
-    // exclusive scans over the lanes (lane 0 holds the top bins)
+    // inclusive scans over the lanes (lane 0 holds the top bins)
     unsigned int bc = lc;
-    double bm = lm;
+    uint64_t bq = lq;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
         const unsigned int tc = __shfl_up_sync(FULL, bc, d);
-        const double tm = __shfl_up_sync(FULL, bm, d);
+        const uint64_t tq = shfl_up_u64(bq, d);
         if (lane >= d) {
             bc += tc;
-            bm += tm;
+            bq += tq;
         }
     }
+    if (rel_p > 0.0) *need_io = rel_p * (static_cast<double>(qbase + shfl_u64(bq, 31)) * inv);
+    const double need = *need_io;
     bc -= lc;
-    bm -= lm;
-    const bool reach = by_mass ? (bm + lm >= need && lc > 0) : (static_cast<int64_t>(bc) + lc >= need_c);
-    uint32_t hit = __ballot_sync(FULL, reach);
-    int L;
-    if (hit) {
-        L = __ffs(hit) - 1;
-    } else {
-        L = 31 - __clz(__ballot_sync(FULL, lc > 0));  // mass short by rounding: the lowest bin with an element
-    }
+    bq -= lq;
+    const bool reach = by_mass ? (static_cast<double>(qbase + bq + lq) * inv >= need && lc > 0)
+                               : (static_cast<int64_t>(bc) + lc >= need_c);
+    const uint32_t hit = __ballot_sync(FULL, reach);
+    const int L = hit ? __ffs(hit) - 1 : 31 - __clz(__ballot_sync(FULL, lc > 0));
     int bin = -1;
     unsigned int ac = 0;
-    double am = 0.0;
+    uint64_t aq = 0;
     if (lane == L) {
         ac = bc;
-        am = bm;
+        aq = bq;
         int last = -1;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             if (bin >= 0) continue;
             if (c8[i] > 0) last = i;
-            const bool r = by_mass ? (am + m8[i] >= need && c8[i] > 0) : (static_cast<int64_t>(ac) + c8[i] >= need_c);
+            const bool r = by_mass ? (static_cast<double>(qbase + aq + q8[i]) * inv >= need && c8[i] > 0)
+                                   : (static_cast<int64_t>(ac) + c8[i] >= need_c);
             if (r) {
                 bin = 255 - (lane * 8 + i);
             } else {
                 ac += c8[i];
-                am += m8[i];
+                aq += q8[i];
             }
         }
-        if (bin < 0) {  // rounding: take the last bin of this lane that holds an element
+        if (bin < 0) {  // short: the last bin of this lane that holds an element
             bin = 255 - (lane * 8 + (last >= 0 ? last : 7));
             ac = bc;
-            am = bm;
+            aq = bq;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
                 if (255 - (lane * 8 + i) > bin) {
                     ac += c8[i];
-                    am += m8[i];
+                    aq += q8[i];
                 }
         }
     }
     bin = __shfl_sync(FULL, bin, L);
     *above_c = __shfl_sync(FULL, ac, L);
-    *above_m = __shfl_sync(FULL, am, L);
+    *above_q = shfl_u64(aq, L);
     return bin;
 }
 
-// Radix select over the ordered keys: the key of the token where the count
-// (by_mass false: the need_c-th token) or the mass (the first token at which
-// the running mass reaches need) is reached, in the order key.  With
-// rel_p > 0, need is rel_p times the row's whole mass, summed in fp64 from
-// the first level's histogram.  Returns the key; *cnt_above / *mass_above:
-// the elements strictly above its value; *ties: how many elements hold its
-// value; *need_used: the mass threshold the select used.  Warp-uniform.
+// Radix select over the value keys: the key where the count (by_mass false:
+// the need_c-th token) or the mass (the first token at which the running
+// mass reaches need; with rel_p > 0, need = rel_p times the row's whole mass,
+// summed exactly by the first pass) is reached.  *cnt_above / *q_above: the
+// elements strictly above its value; *ties: how many hold it; *need_io: the
+// threshold used.  Team-wide.
 template <bool BF16>
-__device__ uint32_t wide_select(ScanSmem &sm, const ScanGeom &g, int64_t row, float m, float c, bool by_mass,
-                                double need, double rel_p, int64_t need_c, int64_t *cnt_above, double *mass_above,
-                                unsigned int *ties, double *need_used, int lane) {
-    const int levels = BF16 ? 2 : 4;  // bf16 keys live in the top 16 bits
+__device__ uint32_t wide_select(const Team &tm, ScanSmem &sm, const ScanGeom &g, int64_t row, float m, float c,
+                                int fxs, bool by_mass, double *need_io, double rel_p, int64_t need_c,
+                                int64_t *cnt_above, uint64_t *q_above, int64_t *ties, int lane) {
+    constexpr int kbits = BF16 ? 16 : 32;
+    const float scale = fx_scale(fxs);
+    const double inv = fx_inv(fxs);
     uint32_t prefix = 0;
     int64_t ca = 0;
-    double ma = 0.0;
-    int bin = 0;
-    for (int L = 0; L < levels; ++L) {
-        const int shift = 24 - 8 * L;
-        wide_hist<BF16>(g, row, prefix, shift, m, c, sm.wide, lane);
-        if (L == 0 && rel_p > 0.0) {
-            double tot = 0.0;
-            for (int i = lane; i < 256; i += 32) tot += sm.wide.mass[i];
-#pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) tot += __shfl_xor_sync(FULL, tot, d);
-            need = rel_p * tot;
-        }
+    uint64_t qa = 0;
+    for (int shift = kbits - 8; shift >= 0; shift -= 8) {
+        wide_hist<BF16>(tm, g, row, prefix, shift, m, c, scale, sm.wide, lane);
         int64_t ac;
-        double am;
-        bin = wide_pick(sm.wide, by_mass, need - ma, need_c - ca, &ac, &am, lane);
+        uint64_t aq;
+        const int bin = wide_pick(sm.wide, by_mass, need_io, shift == kbits - 8 ? rel_p : 0.0, need_c - ca, qa, inv,
+                                  &ac, &aq, lane);
+        if (shift == 0) *ties = sm.wide.cnt[bin];
+        tm.sync();  // every warp read the histogram before the next pass clears it
         ca += ac;
-        ma += am;
+        qa += aq;
         prefix = (prefix << 8) | static_cast<uint32_t>(bin);
     }
     *cnt_above = ca;
-    *mass_above = ma;
-    *need_used = need;
-    *ties = sm.wide.cnt[bin];
-    __syncwarp();
-    return prefix << (32 - 8 * levels);
+    *q_above = qa;
+    return prefix;
 }
 
-// The id of the n-th (from 1) lowest-id element whose ordered value key is
-// vkey: a count select over ~id, four passes.  Warp-uniform.
+// The cut when the 64 best keys of the row (`list`, R = 2) decide it: no
+// filter, or top_p alone with its cut within them (threshold top_p times
+// the scan's total S_all).  Returns false when passes are needed.  Warp.
 template <bool BF16>
-__device__ uint32_t wide_tie_id(ScanSmem &sm, const ScanGeom &g, int64_t row, uint32_t vkey, int64_t n, int lane) {
-    uint32_t prefix = 0;
-    int64_t ca = 0;
-    for (int L = 0; L < 4; ++L) {
-        const int shift = 24 - 8 * L;
-        wide_hist_id<BF16>(g, row, vkey, prefix, shift, sm.wide, lane);
-        int64_t ac;
-        double am;
-        const int bin = wide_pick(sm.wide, false, 0.0, n - ca, &ac, &am, lane);
-        ca += ac;
-        prefix = (prefix << 8) | static_cast<uint32_t>(bin);
-    }
-    return ~prefix;
-}
-
-// The order key of the last kept token when the cut keeps n_t of the ties
-// at ordered value key vkey (ties kept lowest id first).
-template <bool BF16>
-__device__ uint64_t wide_boundary(ScanSmem &sm, const ScanGeom &g, int64_t row, uint32_t vkey, int64_t n_t,
-                                  unsigned int ties, int lane) {
-    if (n_t >= static_cast<int64_t>(ties)) return static_cast<uint64_t>(vkey) << 32;  // every tie kept
-    const uint32_t id = wide_tie_id<BF16>(sm, g, row, vkey, n_t, lane);
-    return (static_cast<uint64_t>(vkey) << 32) | static_cast<uint32_t>(~id);
-}
-
-// The wide filter's cut for a row with maximum m (raw), total mass S_all
-// relative to it, top_k = ek (<= V; > 64) and top_p = tp, given its 64 best
-// keys in `list` (R = 2).  Warp-uniform; the completion warp only.
-template <bool BF16>
-__device__ WideCut wide_cut(ScanSmem &sm, const ScanGeom &g, int64_t row, const WarpList<2> &list, float m,
-                            float S_all, float c, int64_t ek, float tp, bool want_key, int lane) {
+__device__ bool wide_cut_list(const WarpList<2> &list, float m, float S_all, float c, int64_t ek, float tp,
+                              int64_t V, WideCut *out, int lane) {
     WideCut w;
-    w.key_cut = 0;
-    w.cut = g.V;
+    w.cut = V;
     w.P = S_all;
-    const bool top_k = ek < g.V;
-    if (!top_k && !(tp < 1.0f)) return w;  // no filter: the whole row
-    if (!top_k) {
-        // top_p alone: does the cut fall within the 64 best?
-        float e[2];
+    w.all = true;
+    w.vk = 0;
+    w.nkeep = 0;
+    w.ties = INT64_MAX;
+    *out = w;
+    if (ek < V) return false;
+    if (!(tp < 1.0f)) return true;  // no filter: the whole row
+    float e[2];
 #pragma unroll
-        for (int r = 0; r < 2; ++r) e[r] = list.k[r] ? ex2((key_val(list.k[r]) - m) * c) : 0.0f;
-        const float thr = tp * S_all;
-        float base = 0.0f;
+    for (int r = 0; r < 2; ++r) e[r] = list.k[r] ? ex2((key_val(list.k[r]) - m) * c) : 0.0f;
+    const float thr = tp * S_all;
+    float base = 0.0f;
 #pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            float cum = e[r];
+    for (int r = 0; r < 2; ++r) {
+        float cum = e[r];
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const float t = __shfl_up_sync(FULL, cum, d);
-                if (lane >= d) cum += t;
-            }
-            cum += base;
-            const uint32_t hit = __ballot_sync(FULL, list.k[r] != 0 && cum >= thr);
-            if (hit) {
-                const int j = __ffs(hit) - 1;
-                w.cut = r * 32 + j + 1;
-                w.P = __shfl_sync(FULL, cum, j);
-                w.key_cut = list.at(static_cast<int>(w.cut) - 1);
-                return w;
-            }
-            base = __shfl_sync(FULL, cum, 31);
+        for (int d = 1; d < 32; d <<= 1) {
+            const float t = __shfl_up_sync(FULL, cum, d);
+            if (lane >= d) cum += t;
         }
+        cum += base;
+        const uint32_t hit = __ballot_sync(FULL, list.k[r] != 0 && cum >= thr);
+        if (hit) {
+            const int j = __ffs(hit) - 1;
+            w.cut = r * 32 + j + 1;
+            w.P = __shfl_sync(FULL, cum, j);
+            w.all = false;
+            w.vk = wide_vk<BF16>(key_val(list.at(static_cast<int>(w.cut) - 1)));
+            // the list holds the lowest ids of a value first: the kept ties are
+            // the list's entries of value vk before the cut
+            int64_t nk = 0, nt = 0;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const bool same = list.k[rr] != 0 && wide_vk<BF16>(key_val(list.k[rr])) == w.vk;
+                nk += __popc(__ballot_sync(FULL, same && rr * 32 + lane < w.cut));
+                nt += __popc(__ballot_sync(FULL, same));
+            }
+            w.nkeep = nk;
+            // ties past the list's end are not known
+            const uint64_t last = list.at(DFLASH2_MAX_TOPK - 1);
+            w.ties = last != 0 && wide_vk<BF16>(key_val(last)) == w.vk ? INT64_MAX : nt;
+            *out = w;
+            return true;
+        }
+        base = __shfl_sync(FULL, cum, 31);
     }
-    double S_k = S_all;
-    uint32_t key_k = 0;
+    return false;
+}
+
+// The cut by passes over the row for top_k = ek (<= V) and top_p = tp, the
+// row's maximum m (raw) and c = log2(e) / T.  Team-wide.
+template <bool BF16>
+__device__ __noinline__ WideCut wide_cut_passes(const Team &tm, ScanSmem &sm, const ScanGeom &g, int64_t row, float m, float c,
+                                   int64_t ek, float tp, int lane) {
+    const int fxs = wide_fxs(g.V);
+    const float scale = fx_scale(fxs);
+    const double inv = fx_inv(fxs);
+    WideCut w;
+    w.cut = g.V;
+    w.P = NAN;
+    w.all = true;
+    w.vk = 0;
+    w.nkeep = 0;
+    w.ties = INT64_MAX;
+    const bool top_k = ek < g.V;
+    uint64_t Sq = 0;
+    uint32_t vk_k = 0;
     int64_t n_tk = 0;
     if (top_k) {
-        int64_t ca;
-        double ma;
-        unsigned int ties;
-        double unused;
-        key_k = wide_select<BF16>(sm, g, row, m, c, false, 0.0, 0.0, ek, &ca, &ma, &ties, &unused, lane);
+        int64_t ca, ties;
+        uint64_t qa;
+        double unused = 0.0;
+        vk_k = wide_select<BF16>(tm, sm, g, row, m, c, fxs, false, &unused, 0.0, ek, &ca, &qa, &ties, lane);
         n_tk = ek - ca;
-        S_k = ma + static_cast<double>(n_tk) * ex2((ord2f(key_k) - m) * c);
+        const uint64_t qk = wide_q(ex2((wide_vval<BF16>(vk_k) - m) * c), scale);
+        Sq = qa + static_cast<uint64_t>(n_tk) * qk;
         w.cut = ek;
-        w.P = static_cast<float>(S_k);
-        if (want_key && !(tp < 1.0f)) w.key_cut = wide_boundary<BF16>(sm, g, row, key_k, n_tk, ties, lane);
+        w.P = static_cast<float>(static_cast<double>(Sq) * inv);
+        w.all = false;
+        w.vk = vk_k;
+        w.nkeep = n_tk;
+        w.ties = ties;
     }
     if (tp < 1.0f) {
-        // top_k off: the threshold is top_p of the whole row's mass, summed in fp64 by the select's
-        // first pass (the scan's fp32 sum is coarser than the mass of a token near a deep cut)
-        double thr = static_cast<double>(tp) * S_k;
-        int64_t ca;
-        double ma;
-        unsigned int ties;
-        const uint32_t key_p = wide_select<BF16>(sm, g, row, m, c, true, thr, top_k ? 0.0 : static_cast<double>(tp), 0,
-                                                 &ca, &ma, &ties, &thr, lane);
-        if (!top_k || key_p >= key_k) {
-            const double wp = ex2((ord2f(key_p) - m) * c);
-            int64_t n_tp = wp > 0.0 ? static_cast<int64_t>(ceil((thr - ma) / wp)) : 1;
+        // the threshold: top_p of the mass the top_k cut kept, or of the whole
+        // row summed exactly by the select's first pass
+        double thr = top_k ? static_cast<double>(tp) * (static_cast<double>(Sq) * inv) : 0.0;
+        int64_t ca, ties;
+        uint64_t qa;
+        const uint32_t vk_p = wide_select<BF16>(tm, sm, g, row, m, c, fxs, true, &thr,
+                                                top_k ? 0.0 : static_cast<double>(tp), 0, &ca, &qa, &ties, lane);
+        if (!top_k || vk_p >= vk_k) {
+            const uint64_t qp = wide_q(ex2((wide_vval<BF16>(vk_p) - m) * c), scale);
+            const double wp = static_cast<double>(qp) * inv;
+            int64_t n_tp = wp > 0.0 ? static_cast<int64_t>(ceil((thr - static_cast<double>(qa) * inv) / wp)) : 1;
             if (n_tp < 1) n_tp = 1;
-            if (n_tp > static_cast<int64_t>(ties)) n_tp = ties;
-            if (top_k && key_p == key_k && n_tp > n_tk) n_tp = n_tk;
+            if (n_tp > ties) n_tp = ties;
+            if (top_k && vk_p == vk_k && n_tp > n_tk) n_tp = n_tk;
             w.cut = ca + n_tp;
-            w.P = static_cast<float>(ma + static_cast<double>(n_tp) * wp);
-            if (want_key) w.key_cut = wide_boundary<BF16>(sm, g, row, key_p, n_tp, ties, lane);
-        } else if (want_key) {
-            // rounding put the top_p cut below the top_k-th token: keep the top_k cut
-            unsigned int tk_ties = 0;
-            int64_t ca2;
-            double ma2, unused;
-            const uint32_t kk = wide_select<BF16>(sm, g, row, m, c, false, 0.0, 0.0, ek, &ca2, &ma2, &tk_ties, &unused,
-                                                  lane);
-            w.key_cut = wide_boundary<BF16>(sm, g, row, kk, ek - ca2, tk_ties, lane);
-        }
+            w.P = static_cast<float>(static_cast<double>(qa + static_cast<uint64_t>(n_tp) * qp) * inv);
+            w.all = false;
+            w.vk = vk_p;
+            w.nkeep = n_tp;
+            w.ties = ties;
+        }  // else rounding put the top_p cut below the top_k-th token: the top_k cut stands
     }
     return w;
+}
+
+// Where token z of the row stands against the cut: 1 above it (kept), 0
+// below, 2 a tie at the cut's value (kept if its rank among the ties, by id,
+// is below nkeep).
+template <bool BF16>
+__device__ __forceinline__ int wide_side(const WideCut &wc, float z) {
+    if (wc.all) return 1;
+    const uint32_t k = wide_vk<BF16>(z);
+    return k > wc.vk ? 1 : (k == wc.vk ? (wc.nkeep >= wc.ties ? 1 : 2) : 0);
 }
 
 }  // namespace dfl
