@@ -60,7 +60,6 @@ constexpr int VEC_PER_CHUNK = CHUNK_BYTES / 16;
 constexpr int VEC_PER_LANE = VEC_PER_CHUNK / 32;
 constexpr int RING = 128;             // slice-key ring of a streaming warp (a power of two)
 constexpr int GCAP = 128;             // element keys the completion warp gathers at once (its scratch)
-constexpr int WIDE_QCAP = 64;        // wide rows a CTA defers to its epilogue
 constexpr int MAX_SCAN_GRID = 1024;   // CTAs of a scan launch (partial records are sized for it)
 constexpr long long WAIT_CYCLES = 4000000000ll;  // ~2 s at 2 GHz
 constexpr long long DRAIN_CYCLES = 200000000ll;  // ~0.1 s
@@ -93,21 +92,27 @@ struct PartRec {
     uint64_t keys[DFLASH2_MAX_TOPK];  // best keys, descending (keys[0] = best for an argmax)
 };
 
+// A scan's workspace: one ticket per row, one wide mark per row (the CTA,
+// plus one, that left the row to its epilogue), the partial records of
+// split rows.  Tickets and marks are zero between calls.
 struct ScanWs {
-    int32_t *tickets;  // [rows], zero between calls
+    int32_t *tickets;  // [rows]
+    int32_t *marks;    // [rows]
     PartRec *parts;    // [2 * MAX_SCAN_GRID]
 };
 
-inline size_t scan_ws_tickets_bytes(int64_t rows) {
+constexpr size_t scan_ws_rows_bytes(int64_t rows) {
     return (static_cast<size_t>(rows) * sizeof(int32_t) + 255) / 256 * 256;
 }
-inline size_t scan_ws_bytes(int64_t rows) {
-    return scan_ws_tickets_bytes(rows) + static_cast<size_t>(2 * MAX_SCAN_GRID) * sizeof(PartRec);
+constexpr size_t scan_ws_bytes(int64_t rows) {
+    return 2 * scan_ws_rows_bytes(rows) + static_cast<size_t>(2 * MAX_SCAN_GRID) * sizeof(PartRec);
 }
 inline ScanWs scan_ws_at(void *p, int64_t rows) {
+    char *c = static_cast<char *>(p);
     ScanWs w;
-    w.tickets = static_cast<int32_t *>(p);
-    w.parts = reinterpret_cast<PartRec *>(static_cast<char *>(p) + scan_ws_tickets_bytes(rows));
+    w.tickets = reinterpret_cast<int32_t *>(c);
+    w.marks = reinterpret_cast<int32_t *>(c + scan_ws_rows_bytes(rows));
+    w.parts = reinterpret_cast<PartRec *>(c + 2 * scan_ws_rows_bytes(rows));
     return w;
 }
 
@@ -145,6 +150,7 @@ struct ScanSmem {
     unsigned int ring_head[SCAN_WARPS];    // keys pushed to each warp's ring so far
     unsigned int ring_tail[SCAN_WARPS];    // keys of each ring the completion warp has taken
     int ngather;                           // keys the completion warp has gathered into its scratch
+    int nwide;                             // rows the completion warp left to the epilogue
     uint32_t lmax[2][SCAN_WARPS][DFLASH2_MAX_TOPK];  // sorted half-slice maxima of each warp's first chunk of a row
     uint64_t ring[SCAN_WARPS][RING];       // slice keys, position = count mod RING
     // Row results handed from the streaming warps to the completion warp.
@@ -155,19 +161,6 @@ struct ScanSmem {
         unsigned int ring_end[SCAN_WARPS];  // 1 + the warp's ring count at its end of the row; 0 before
     } hand[2];
     alignas(16) unsigned char scratch[GCAP * 8];  // the completion warp's gathered keys; verify's draws
-    // Wide rows (a filter that reaches past the 64 best): the passes'
-    // histogram, and the rows whose passes wait for the CTA's epilogue.
-    struct WideHist {
-        union {
-            struct {
-                unsigned int lo[256], hi[256];  // fixed-point masses as 32-bit halves
-            } fx;
-            double blk[256];                    // a draw's block masses
-        } u;
-        unsigned int cnt[256];                  // counts (a draw's ties per block)
-        int nq;                                 // rows deferred to the epilogue
-        int q[WIDE_QCAP];                       // their index relative to the CTA's first row
-    } wide;
     alignas(128) unsigned char buf[SCAN_WARPS][WSTAGES][CHUNK_BYTES];
 };
 
@@ -1119,7 +1112,7 @@ __device__ __forceinline__ void scan_init(ScanSmem &sm) {
             mbar_init(&sm.slot_empty[s], 1);
         }
         sm.floor_ord[0] = sm.floor_ord[1] = 0;
-        sm.wide.nq = 0;
+        sm.nwide = 0;
         for (int w = 0; w < SCAN_WARPS; ++w) {
             sm.ring_head[w] = sm.ring_tail[w] = 0;
             sm.hand[0].ring_end[w] = sm.hand[1].ring_end[w] = 0;

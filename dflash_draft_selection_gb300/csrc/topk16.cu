@@ -58,27 +58,25 @@ __device__ __forceinline__ void finalize_draft(const RowResult<R> &res, const Ro
     if (lane == 0) lse[row] = L;
 }
 
-// A wide row whose cut needs passes waits for the CTA's epilogue: its ids
-// go out now, its logits (in cand_U) and maximum (in lse) until then.
+// A wide row whose cut needs passes over the row is left to the CTA's
+// epilogue: its ids go out now, its logits (in cand_U) and maximum (in lse)
+// until then, and the row is marked as this CTA's.
 template <int R>
-__device__ __forceinline__ void defer_draft(ScanSmem &sm, const RowResult<R> &res, int64_t row, int rrel,
+__device__ __forceinline__ void defer_draft(ScanSmem &sm, const ScanWs &sw, const RowResult<R> &res, int64_t row,
                                             int32_t *cand_idx, float *cand_U, float *lse, int lane) {
     const uint64_t k = res.list.k[0];
     if (lane < NC) {
         cand_idx[row * NC + lane] = key_idx(k);
         cand_U[row * NC + lane] = key_val(k);
     }
-    const int n = sm.wide.nq;
-    __syncwarp();
     if (lane == 0) {
         lse[row] = res.m;
-        sm.wide.q[n] = rrel;
-        sm.wide.nq = n + 1;
+        sw.marks[row] = static_cast<int32_t>(blockIdx.x) + 1;
+        ++sm.nwide;
     }
-    __syncwarp();
 }
 
-// The epilogue's outputs of a deferred row (as finalize_draft writes them).
+// The epilogue's outputs of a marked row (as finalize_draft writes them).
 __device__ __forceinline__ void finalize_deferred(const RowTask &task, int64_t row, float m, const WideCut &wc,
                                                   float *cand_U, float *lse, int lane) {
     const float lns = logf(wc.P);
@@ -87,6 +85,45 @@ __device__ __forceinline__ void finalize_deferred(const RowTask &task, int64_t r
         cand_U[row * NC + lane] = lane < wc.cut ? (z - m) / task.T - lns : NEG_INF;
     }
     if (lane == 0) lse[row] = m / task.T + lns;
+}
+
+// A completed row whose filter may reach past its 64 best: the cut from the
+// list when it decides it, else the row is left to the epilogue.
+template <int R, bool BF16>
+__device__ __forceinline__ void draft_wide_done(ScanSmem &sm, const ScanGeom &g, const ScanWs &sw,
+                                                const RowResult<R> &res, const RowTask &task, int64_t row,
+                                                int32_t *cand_idx, float *cand_U, float *lse, int lane) {
+    WideCut wc;
+    wc.cut = 0;
+    wc.P = NAN;
+    if constexpr (R == 2) {
+        if (!res.bad && isfinite(res.m) &&
+            !wide_cut_list<BF16>(res.list, res.m, res.s, LOG2E / task.T, task.ek, task.top_p, g.V, &wc, lane)) {
+            defer_draft<R>(sm, sw, res, row, cand_idx, cand_U, lse, lane);
+            return;
+        }
+    }
+    finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane, &wc);
+}
+
+// The rows this CTA marked, on all five warps once the CTA has streamed its
+// range: the cut by passes over the row, then the row's U and lse.
+template <bool BF16>
+__device__ __forceinline__ void draft_epilogue(ScanSmem &ssm, const ScanGeom g, const ScanWs sw, int64_t r_first,
+                                            int64_t r_last, float *cand_U, float *lse) {
+    WideSmem &sm = wide_smem(ssm);
+    const Team tm{static_cast<int>(threadIdx.x), SCAN_THREADS};
+    const int lane = threadIdx.x & 31;
+    const int32_t me = static_cast<int32_t>(blockIdx.x) + 1;
+    for (int64_t row = r_first; row <= r_last; ++row) {
+        if (sw.marks[row] != me) continue;  // the same for every thread: only this CTA writes `me`
+        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V_params, false);
+        const float m = lse[row];
+        const WideCut wc = wide_cut_passes<BF16>(tm, sm, g, row, m, LOG2E / task.T, task.ek, task.top_p, lane);
+        if (tm.warp() == 0) finalize_deferred(task, row, m, wc, cand_U, lse, lane);
+        tm.sync();
+        if (threadIdx.x == 0) sw.marks[row] = 0;
+    }
 }
 
 // Outputs of a vocabulary shard's partial (dflash2_topk16_shard); part_idx
@@ -340,27 +377,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
                 if (so.part_idx) {
                     finalize_shard<R>(res, task, row, so, lane);
                 } else if (task.wide) {
-                    // a filter that may reach past the 64 best: the cut from the
-                    // list, else passes over the row, in the epilogue if the queue
-                    // has room
-                    WideCut wc;
-                    wc.cut = 0;
-                    wc.P = NAN;
-                    bool ready = true;
-                    if constexpr (R == 2) {
-                        const float c = LOG2E / task.T;
-                        if (!res.bad && isfinite(res.m) &&
-                            !wide_cut_list<BF16>(res.list, res.m, res.s, c, task.ek, task.top_p, g.V, &wc, lane)) {
-                            if (sm.wide.nq < WIDE_QCAP) {
-                                defer_draft<R>(sm, res, row, rrel, cand_idx, cand_U, lse, lane);
-                                ready = false;
-                            } else {
-                                wc = wide_cut_passes<BF16>(Team{lane, 32}, sm, g, row, res.m, c, task.ek, task.top_p,
-                                                           lane);
-                            }
-                        }
-                    }
-                    if (ready) finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane, &wc);
+                    draft_wide_done<R, BF16>(sm, g, sw, res, task, row, cand_idx, cand_U, lse, lane);
                 } else {
                     finalize_draft<R>(res, task, row, cand_idx, cand_U, lse, lane);
                 }
@@ -368,19 +385,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED>()) k_to
         }
     }
     if constexpr (SAMPLED) {
-        // the deferred wide rows, on all five warps
-        __syncthreads();
-        const Team tm{static_cast<int>(threadIdx.x), SCAN_THREADS};
-        const int nq = sm.wide.nq;
-        for (int i = 0; i < nq; ++i) {
-            const int64_t row = r_first + sm.wide.q[i];
-            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V_params, false);
-            const float m = lse[row];
-            const WideCut wc =
-                wide_cut_passes<BF16>(tm, sm, g, row, m, LOG2E / task.T, task.ek, task.top_p, lane);
-            if (w == 0) finalize_deferred(task, row, m, wc, cand_U, lse, lane);
-            tm.sync();
-        }
+        __syncthreads();  // the stream buffers are idle from here
+        if (sm.nwide > 0) draft_epilogue<BF16>(sm, g, sw, r_first, r_last, cand_U, lse);
     }
 }
 
@@ -441,7 +447,10 @@ static dflash2_status topk16_call(const void *logits, dflash2_dtype dt, int64_t 
     ScanGeom g = make_geom(logits, ld, es, V, rows, params, rows_per_param);
     if (V_params > 0) g.V_params = V_params;
     const ScanWs sw = scan_ws_at(ws, rows);
-    if (clear_tickets && cudaMemsetAsync(sw.tickets, 0, static_cast<size_t>(rows) * sizeof(int32_t), s) != cudaSuccess)
+    // the tickets and the wide marks, one range
+    if (clear_tickets &&
+        cudaMemsetAsync(sw.tickets, 0, scan_ws_rows_bytes(rows) + static_cast<size_t>(rows) * sizeof(int32_t), s) !=
+            cudaSuccess)
         return DFLASH2_ERR_CUDA;
     if (params == nullptr)
         return dt == DFLASH2_BF16 ? launch_topk16<false, true>(g, sw, cand_idx, cand_U, lse, so, s)
@@ -466,10 +475,9 @@ extern "C" dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, i
 namespace dfl {
 
 constexpr int64_t TOPK_NOALLOC_MAX_ROWS = DFLASH2_TOPK16_NOALLOC_MAX_ROWS;
-constexpr size_t TOPK_NOALLOC_BYTES =
-    (TOPK_NOALLOC_MAX_ROWS * sizeof(int32_t) + 255) / 256 * 256 + static_cast<size_t>(2 * MAX_SCAN_GRID) * sizeof(PartRec);
+constexpr size_t TOPK_NOALLOC_BYTES = scan_ws_bytes(TOPK_NOALLOC_MAX_ROWS);
 
-// Every GPU that loads the library holds this array (about 1.1 MB) until the
+// Every GPU that loads the library holds this array (about 1.2 MB) until the
 // process exits.  All calls share it.
 static __device__ __align__(256) unsigned char g_topk_noalloc_ws[TOPK_NOALLOC_BYTES];
 
@@ -503,10 +511,11 @@ extern "C" dflash2_status dflash2_topk16_noalloc(const void *logits, dflash2_dty
                            false, s);
     void *ws = dfl::topk_noalloc_ws();
     if (!ws) return DFLASH2_ERR_CUDA;
-    // The tickets of the call's rows must start at zero.  A call leaves them
-    // zero again, but one cut short (a launch error, or a kernel that gave up
-    // on a bounded wait) may not, so every call clears them first.  The
-    // partial records are written before they are read and need no clearing.
+    // The tickets and wide marks of the call's rows must start at zero.  A
+    // call leaves them zero again, but one cut short (a launch error, or a
+    // kernel that gave up on a bounded wait) may not, so every call clears
+    // them first.  The partial records are written before they are read and
+    // need no clearing.
     return topk16_call(logits, dt, rows, V, ld, params, rows_per_param, cand_idx, cand_U, lse, ws,
                        dfl::TOPK_NOALLOC_BYTES, true, s);
 }

@@ -114,6 +114,7 @@ struct DrawScratch {
     int32_t wcand[NC];  // and its id
 };
 static_assert(sizeof(DrawScratch) <= sizeof(ScanSmem::scratch), "the draw scratch fits the completion warp's scratch");
+static_assert(sizeof(DrawScratch) <= sizeof(WideSmem::scratch), "the draw scratch fits the epilogue's scratch");
 
 // Inverse CDF over the entries sorted by ascending token id: the first entry
 // whose running weight exceeds u * (total weight); if rounding leaves none,
@@ -354,12 +355,12 @@ __device__ __forceinline__ WideBlocks wide_blocks(int64_t V) {
 // P (h.u.blk) and the ties at the cut's value in the blocks before it
 // (h.cnt).  Team-wide; ends synchronised.
 template <bool BF16>
-__device__ void wide_block_pass(const Team &tm, ScanSmem &sm, const ScanGeom &g, int64_t row, const WideCut &wc,
-                                float m, float c, float scale, double inv, const WideBlocks &wb, int lane) {
+__device__ void wide_block_pass(const Team &tm, WideSmem &sm, const ScanGeom &g, int64_t row, const WideCut &wc,
+                                float m, float c, const Fx &fx, const WideBlocks &wb, int lane) {
     using VL = VecLoad<BF16>;
     constexpr int VE = VL::VE;
     constexpr int esz = BF16 ? 2 : 4;
-    ScanSmem::WideHist &h = sm.wide;
+    WideHist &h = sm.h;
     for (int i = tm.rank; i < 256; i += tm.size) {
         h.cnt[i] = 0;
         h.u.fx.lo[i] = 0;
@@ -372,7 +373,7 @@ __device__ void wide_block_pass(const Team &tm, ScanSmem &sm, const ScanGeom &g,
     auto tally = [&](float x, bool valid, uint64_t &q, uint32_t &t) {
         if (!valid) return;
         const int s = wc.all ? 1 : (wide_vk<BF16>(x) > wc.vk ? 1 : (wide_vk<BF16>(x) == wc.vk ? 2 : 0));
-        if (s == 1) q += wide_q(ex2((x - m) * c), scale);
+        if (s == 1) q += wide_q(ex2((x - m) * c), fx);
         if (s == 2) ++t;
     };
     auto publish = [&](int64_t e0, uint64_t q, uint32_t t) {  // the warp's 32 vectors lie in one block
@@ -416,7 +417,7 @@ __device__ void wide_block_pass(const Team &tm, ScanSmem &sm, const ScanGeom &g,
     tm.sync();
     // blocks 8 lane .. 8 lane + 7 of every warp: ties before each block, the
     // ties each keeps (the lowest ids first), its mass
-    const uint64_t qcut = wc.all ? 0ull : wide_q(ex2((wide_vval<BF16>(wc.vk) - m) * c), scale);
+    const uint64_t qcut = wc.all ? 0ull : wide_q(ex2((wide_vval<BF16>(wc.vk) - m) * c), fx);
     uint32_t tb[8], own = 0;
     double mb[8];
 #pragma unroll
@@ -438,7 +439,7 @@ __device__ void wide_block_pass(const Team &tm, ScanSmem &sm, const ScanGeom &g,
         const int bi = lane * 8 + i;
         int64_t kept = wc.nkeep - static_cast<int64_t>(before);
         kept = kept < 0 ? 0 : (kept > tb[i] ? tb[i] : kept);
-        mb[i] = bi < wb.nblk ? static_cast<double>(fx_get(h, bi) + static_cast<uint64_t>(kept) * qcut) * inv * invP
+        mb[i] = bi < wb.nblk ? static_cast<double>(fx_get(h, bi) + static_cast<uint64_t>(kept) * qcut) * fx.inv * invP
                              : 0.0;
         const uint32_t t = tb[i];
         tb[i] = before;
@@ -462,7 +463,7 @@ __device__ void wide_block_pass(const Team &tm, ScanSmem &sm, const ScanGeom &g,
 // blocks before v's, then those of v's block before v.  One thread; after
 // the block pass.
 template <bool BF16>
-__device__ int64_t wide_tie_rank(const ScanSmem::WideHist &h, const char *rowp, const WideCut &wc,
+__device__ int64_t wide_tie_rank(const WideHist &h, const char *rowp, const WideCut &wc,
                                  const WideBlocks &wb, int64_t v) {
     const int64_t bi = v / wb.blk;
     int64_t r = h.cnt[bi];
@@ -473,14 +474,14 @@ __device__ int64_t wide_tie_rank(const ScanSmem::WideHist &h, const char *rowp, 
 // p(v) (0 outside the kept set or the vocabulary).  A tie at the cut's
 // value needs the block pass first.  Per thread.
 template <bool BF16>
-__device__ double wide_p(const ScanSmem::WideHist &h, const char *rowp, int64_t V, int32_t v, const WideCut &wc,
-                         float m, float c, float scale, double inv, const WideBlocks &wb) {
+__device__ double wide_p(const WideHist &h, const char *rowp, int64_t V, int32_t v, const WideCut &wc,
+                         float m, float c, const Fx &fx, const WideBlocks &wb) {
     if (v < 0 || v >= V) return 0.0;
     const float z = VecLoad<BF16>::scalar(rowp, v);
     const int s = wide_side<BF16>(wc, z);
     if (s == 0) return 0.0;
     if (s == 2 && wide_tie_rank<BF16>(h, rowp, wc, wb, v) >= wc.nkeep) return 0.0;
-    return static_cast<double>(wide_q(ex2((z - m) * c), scale)) * inv / static_cast<double>(wc.P);
+    return static_cast<double>(wide_q(ex2((z - m) * c), fx)) * fx.inv / static_cast<double>(wc.P);
 }
 
 // Inverse CDF over ascending token ids of r (the residual max(0, p - q) with
@@ -489,15 +490,15 @@ __device__ double wide_p(const ScanSmem::WideHist &h, const char *rowp, int64_t 
 // leaves none, the last token with a positive weight.  After the block
 // pass; every warp of the team computes the same token.
 template <bool BF16>
-__device__ int32_t wide_draw(const Team &tm, ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, int64_t row,
-                             const WideCut &wc, float m, float c, float scale, double inv, const WideBlocks &wb,
+__device__ int32_t wide_draw(const Team &tm, WideSmem &sm, DrawScratch &sc, const ScanGeom &g, int64_t row,
+                             const WideCut &wc, float m, float c, const Fx &fx, const WideBlocks &wb,
                              int32_t cand, float qv, bool has_q, float u, int lane) {
     using VL = VecLoad<BF16>;
-    const ScanSmem::WideHist &h = sm.wide;
+    const WideHist &h = sm.h;
     const char *rowp = g.base + row * g.ld_bytes;
     const int64_t V = g.V;
     // the candidates' p and r, and the residual's total Z = 1 - sum_j min(p_j, q_j)
-    const double pj = has_q && lane < NC ? wide_p<BF16>(h, rowp, V, cand, wc, m, c, scale, inv, wb) : 0.0;
+    const double pj = has_q && lane < NC ? wide_p<BF16>(h, rowp, V, cand, wc, m, c, fx, wb) : 0.0;
     const double rj = has_q && lane < NC ? (pj > qv ? pj - qv : 0.0) : 0.0;
     double mn = has_q && lane < NC ? (pj < qv ? pj : static_cast<double>(qv)) : 0.0;
 #pragma unroll
@@ -581,7 +582,7 @@ __device__ int32_t wide_draw(const Team &tm, ScanSmem &sm, DrawScratch &sc, cons
         const float z = VL::scalar(rowp, e);
         int s = wc.all ? 1 : (wide_vk<BF16>(z) > wc.vk ? 1 : (wide_vk<BF16>(z) == wc.vk ? 2 : 0));
         if (s == 2) s = (!partial || rank < wc.nkeep) ? 1 : 0, ++rank;
-        double r = s == 1 ? static_cast<double>(wide_q(ex2((z - m) * c), scale)) * inv * invP : 0.0;
+        double r = s == 1 ? static_cast<double>(wide_q(ex2((z - m) * c), fx)) * fx.inv * invP : 0.0;
         if (use_cand) {
 #pragma unroll 4
             for (int j = 0; j < NC; ++j)
@@ -637,14 +638,12 @@ __device__ int32_t wide_draw(const Team &tm, ScanSmem &sm, DrawScratch &sc, cons
 // takes them for rows whose p lies in their 64 best).  Team-wide; the
 // record is written by the team's first thread.
 template <bool BF16>
-__device__ __noinline__ void row_decide_wide(const Team &tm, ScanSmem &sm, DrawScratch &sc, const ScanGeom &g,
+__device__ __forceinline__ void row_decide_wide(const Team &tm, WideSmem &sm, DrawScratch &sc, const ScanGeom &g,
                                 const VerifyArgs &a, int64_t row, int64_t b, int t, const WideCut &wc, float m,
                                 float c, TRec *rec, int lane) {
     const int K = a.K;
     const char *rowp = g.base + row * g.ld_bytes;
-    const int fxs = wide_fxs(g.V);
-    const float scale = fx_scale(fxs);
-    const double inv = fx_inv(fxs);
+    const Fx fx = wide_fx(g.V);
     const WideBlocks wb = wide_blocks<BF16>(g.V);
     bool blocks = false;
     int32_t qflag = DFLASH2_ST_OK, accepted = 0, emit = -1;
@@ -665,21 +664,21 @@ __device__ __noinline__ void row_decide_wide(const Team &tm, ScanSmem &sm, DrawS
         }
         if (qflag == DFLASH2_ST_OK) {
             if (d >= 0 && d < g.V && wide_side<BF16>(wc, VecLoad<BF16>::scalar(rowp, d)) == 2) {
-                wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, scale, inv, wb, lane);  // d's rank among the ties
+                wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, fx, wb, lane);  // d's rank among the ties
                 blocks = true;
             }
-            const float pd = static_cast<float>(wide_p<BF16>(sm.wide, rowp, g.V, d, wc, m, c, scale, inv, wb));
+            const float pd = static_cast<float>(wide_p<BF16>(sm.h, rowp, g.V, d, wc, m, c, fx, wb));
             const float qd = a.q_sel[o + js];
             accepted = a.u_acc[b * K + t] * qd < pd ? 1 : 0;
             if (!accepted) {
-                if (!blocks) wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, scale, inv, wb, lane);
-                emit = wide_draw<BF16>(tm, sm, sc, g, row, wc, m, c, scale, inv, wb, cand, qv, true,
+                if (!blocks) wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, fx, wb, lane);
+                emit = wide_draw<BF16>(tm, sm, sc, g, row, wc, m, c, fx, wb, cand, qv, true,
                                        a.u_res[b * (K + 1) + t], lane);
             }
         }
     } else {
-        wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, scale, inv, wb, lane);
-        emit = wide_draw<BF16>(tm, sm, sc, g, row, wc, m, c, scale, inv, wb, -1, 0.0f, false,
+        wide_block_pass<BF16>(tm, sm, g, row, wc, m, c, fx, wb, lane);
+        emit = wide_draw<BF16>(tm, sm, sc, g, row, wc, m, c, fx, wb, -1, 0.0f, false,
                                a.u_res[b * (K + 1) + K], lane);
     }
     if (tm.rank == 0) {
@@ -703,6 +702,64 @@ __device__ void row_done(const VerifyArgs &a, const dflash2_sampling *params, in
         if (lane == 0) a.tickets[b] = 0;  // zero again for the next call
         __syncwarp();
         accept_request<SAMPLED>(a, params, b, V, sc, lane);
+    }
+}
+
+// A completed wide row: its record's flags; the cut from the list when it
+// decides it; the rest (the passes and the decisions) is left to the CTA's
+// epilogue, with the row's state stashed in its record and the row marked
+// as this CTA's.  A bad row's record goes out now.
+template <bool SAMPLED, int R, bool BF16>
+__device__ __forceinline__ void target_wide_done(ScanSmem &sm, DrawScratch &sc, const ScanGeom &g, const ScanWs &sw,
+                                                 const VerifyArgs &a, const RowResult<R> &res, const RowTask &task,
+                                                 int64_t row, TRec *rec, int lane) {
+    const bool bad = res.bad || !isfinite(res.m);
+    if (lane == 0) {
+        rec->n = 0;
+        rec->flags = bad ? DFLASH2_ST_NAN : DFLASH2_ST_OK;
+    }
+    if constexpr (R == 2) {
+        if (!bad) {
+            WideCut wc;
+            const bool ready =
+                wide_cut_list<BF16>(res.list, res.m, res.s, LOG2E / task.T, task.ek, task.top_p, g.V, &wc, lane);
+            if (lane == 0) {
+                stash_put(rec, res.m, ready, wc);
+                sw.marks[row] = static_cast<int32_t>(blockIdx.x) + 1;
+                ++sm.nwide;
+            }
+            return;
+        }
+    }
+    row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
+}
+
+// The rows this CTA marked, on all five warps once the CTA has streamed its
+// range: the cut (unless the 64 best gave it), the row's decisions, then
+// its record goes out (and the request's accept walk, if it was the last
+// row).
+template <bool BF16>
+__device__ __forceinline__ void verify_epilogue(ScanSmem &ssm, const ScanGeom g, const ScanWs sw, const VerifyArgs a,
+                                             int64_t r_first, int64_t r_last) {
+    WideSmem &sm = wide_smem(ssm);
+    DrawScratch &sc = *reinterpret_cast<DrawScratch *>(sm.scratch);
+    const Team tm{static_cast<int>(threadIdx.x), SCAN_THREADS};
+    const int lane = threadIdx.x & 31;
+    const int32_t me = static_cast<int32_t>(blockIdx.x) + 1;
+    for (int64_t row = r_first; row <= r_last; ++row) {
+        if (sw.marks[row] != me) continue;  // the same for every thread: only this CTA writes `me`
+        const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
+        const float cw = LOG2E / task.T;
+        TRec *rec = a.recs + row;
+        WideCut wc;
+        const WideStash st = stash_get(rec, &wc);
+        if (!st.ready) wc = wide_cut_passes<BF16>(tm, sm, g, row, st.m, cw, task.ek, task.top_p, lane);
+        row_decide_wide<BF16>(tm, sm, sc, g, a, row, row / (a.K + 1), static_cast<int>(row % (a.K + 1)), wc, st.m,
+                              cw, rec, lane);
+        tm.sync();
+        if (tm.warp() == 0) row_done<true>(a, g.params, row, g.V, sc, lane);
+        tm.sync();
+        if (threadIdx.x == 0) sw.marks[row] = 0;
     }
 }
 
@@ -767,40 +824,7 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()
                 take_row<R, MODE_TOPN_LSE, BF16>(sm, g, row, res, rrel, cw, task.nsel, tail, aborted, lane, &g_err_verify);
                 done = join_parts<R, MODE_TOPN_LSE>(g, sw, row, res, cw, lane);
                 if (done && !res.bad) res.list = extract_topn<R, BF16>(g, row, res.list, task.nsel, sm.scratch, &sm.ngather, lane);
-                if (done) {
-                    const bool bad = res.bad || !isfinite(res.m);
-                    if (lane == 0) {
-                        rec->n = 0;
-                        rec->flags = bad ? DFLASH2_ST_NAN : DFLASH2_ST_OK;
-                    }
-                    bool decided = true;
-                    if constexpr (R == 2) {
-                        if (!bad) {
-                            // the cut from the list when it decides it; the passes and
-                            // the draws in the epilogue if the queue has room
-                            WideCut wc;
-                            const bool ready =
-                                wide_cut_list<BF16>(res.list, res.m, res.s, cw, task.ek, task.top_p, g.V, &wc, lane);
-                            const int n = sm.wide.nq;
-                            if (n < WIDE_QCAP) {
-                                __syncwarp();
-                                if (lane == 0) {
-                                    stash_put(rec, res.m, ready, wc);
-                                    sm.wide.q[n] = rrel;
-                                    sm.wide.nq = n + 1;
-                                }
-                                __syncwarp();
-                                decided = false;
-                            } else {
-                                const Team t1{lane, 32};
-                                if (!ready) wc = wide_cut_passes<BF16>(t1, sm, g, row, res.m, cw, task.ek, task.top_p, lane);
-                                row_decide_wide<BF16>(t1, sm, sc, g, a, row, row / (a.K + 1),
-                                                      static_cast<int>(row % (a.K + 1)), wc, res.m, cw, rec, lane);
-                            }
-                        }
-                    }
-                    if (decided) row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
-                }
+                if (done) target_wide_done<SAMPLED, R, BF16>(sm, sc, g, sw, a, res, task, row, rec, lane);
                 continue;
             } else {
                 take_row<R, MODE_ARGMAX, BF16>(sm, g, row, res, rrel, LOG2E, task.nsel, tail, aborted, lane, &g_err_verify);
@@ -825,25 +849,8 @@ __global__ void __launch_bounds__(SCAN_THREADS, scan_min_blocks<SAMPLED, true>()
         }
     }
     if constexpr (SAMPLED) {
-        // the deferred wide rows, on all five warps; the completion warp
-        // then publishes each row's record
-        __syncthreads();
-        const Team tm{static_cast<int>(threadIdx.x), SCAN_THREADS};
-        const int nq = sm.wide.nq;
-        for (int i = 0; i < nq; ++i) {
-            const int64_t row = r_first + sm.wide.q[i];
-            const RowTask task = decode_row(g.params, row / g.rows_per_param, g.V, true);
-            const float cw = LOG2E / task.T;
-            TRec *rec = a.recs + row;
-            WideCut wc;
-            const WideStash st = stash_get(rec, &wc);
-            if (!st.ready) wc = wide_cut_passes<BF16>(tm, sm, g, row, st.m, cw, task.ek, task.top_p, lane);
-            row_decide_wide<BF16>(tm, sm, sc, g, a, row, row / (a.K + 1), static_cast<int>(row % (a.K + 1)), wc,
-                                  st.m, cw, rec, lane);
-            tm.sync();
-            if (w == SCAN_WARPS) row_done<SAMPLED>(a, g.params, row, g.V, sc, lane);
-            tm.sync();
-        }
+        __syncthreads();  // the stream buffers are idle from here
+        if (sm.nwide > 0) verify_epilogue<BF16>(sm, g, sw, a, r_first, r_last);
     }
 }
 
