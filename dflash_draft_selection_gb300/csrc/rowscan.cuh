@@ -59,7 +59,7 @@ constexpr int SCAN_THREADS = SCAN_WARPS * 32 + 32;  // + one completion warp
 constexpr int VEC_PER_CHUNK = CHUNK_BYTES / 16;
 constexpr int VEC_PER_LANE = VEC_PER_CHUNK / 32;
 constexpr int RING = 128;             // slice-key ring of a streaming warp (a power of two)
-constexpr int GCAP = 128;             // element keys the completion warp gathers at once (its scratch)
+constexpr int GCAP = 256;             // element keys the completion warp gathers at once (its scratch)
 constexpr int MAX_SCAN_GRID = 1024;   // CTAs of a scan launch (partial records are sized for it)
 constexpr long long WAIT_CYCLES = 4000000000ll;  // ~2 s at 2 GHz
 constexpr long long DRAIN_CYCLES = 200000000ll;  // ~0.1 s
@@ -1024,12 +1024,74 @@ __device__ __forceinline__ WarpList<R> extract_topn(const ScanGeom &g, int64_t r
             }
         }
         __syncwarp();
-        const int total = *reinterpret_cast<volatile int *>(ngather);
+        // one read, broadcast: every lane takes the same branch, and all have
+        // read the cursor before lane 0 resets it below
+        const int total = __shfl_sync(FULL, *reinterpret_cast<volatile int *>(ngather), 0);
         if (total <= GCAP) {
             merge_buffer<R>(out, gbuf, total, lane);
             return out;
         }
     }
+    // A slice tied at F may have been left out of the list (always possible
+    // when the list is exactly N long), or the listed slices held more than
+    // the scratch: gather every element of the row that reaches F, in one
+    // pass (a vector whose maximum falls below F adds nothing).
+    if (lane == 0) *ngather = 0;
+    __syncwarp();
+#pragma unroll 1
+    for (int c = 0; c < g.cpr; ++c) {
+        const int nvt = static_cast<int>(chunk_bulk_bytes(g, c)) >> 4;
+        const uint32_t cb = static_cast<uint32_t>(c) * CE;
+        const uint4 *cp = reinterpret_cast<const uint4 *>(rowp + static_cast<int64_t>(cb) * esz);
+        uint4 v[VEC_PER_LANE];
+#pragma unroll
+        for (int q = 0; q < VEC_PER_LANE; ++q)
+            v[q] = q * 32 + lane < nvt ? __ldcs(cp + q * 32 + lane)
+                                       : make_uint4(VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD, VL::NEG_WORD);
+        uint32_t qm = 0;
+#pragma unroll
+        for (int q = 0; q < VEC_PER_LANE; ++q)
+            if (q * 32 + lane < nvt && VL::vmax(v[q]) >= F) qm |= 1u << q;
+#pragma unroll 1
+        while (qm) {
+            const int q = __ffs(qm) - 1;
+            qm &= qm - 1;
+            uint4 u = v[0];
+#pragma unroll
+            for (int j = 1; j < VEC_PER_LANE; ++j)
+                if (j == q) u = v[j];
+            float x[VE];
+            VL::unpack(u, x);
+            const uint32_t i0 = cb + static_cast<uint32_t>((q * 32 + lane) * VE);
+#pragma unroll
+            for (int e = 0; e < VE; ++e) {
+                if (x[e] >= F) {
+                    const int pos = atomicAdd(ngather, 1);
+                    if (pos < GCAP) gbuf[pos] = make_key(x[e], i0 + e);
+                }
+            }
+        }
+    }
+    {
+        const int64_t t0 = static_cast<int64_t>(g.cpr - 1) * CE + chunk_bulk_bytes(g, g.cpr - 1) / esz;
+        for (int64_t i = t0 + lane; i < g.V; i += 32) {
+            const float x = VL::scalar(rowp, i);
+            if (x >= F) {
+                const int pos = atomicAdd(ngather, 1);
+                if (pos < GCAP) gbuf[pos] = make_key(x, static_cast<uint32_t>(i));
+            }
+        }
+    }
+    __syncwarp();
+    {
+        const int total = __shfl_sync(FULL, *reinterpret_cast<volatile int *>(ngather), 0);
+        if (total <= GCAP) {
+            out.clear();
+            merge_buffer<R>(out, gbuf, total, lane);
+            return out;
+        }
+    }
+    // more elements reach F than the scratch holds: rank every slice
     for (int c = 0; c < g.cpr; ++c) {
         const uint32_t base = static_cast<uint32_t>(c) * CE + lane * VE;
         const bool take = lane * 16 < static_cast<int>(chunk_bulk_bytes(g, c));
