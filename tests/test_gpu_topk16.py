@@ -164,6 +164,23 @@ def test_wide_filters(ref, dtype):
     assert deep.any() and (~deep).any()
 
 
+def test_exactly_64_with_ties_at_f(ref):
+    """Lists exactly 64 long (top_k = 64, and top_p with top_k off) on rows whose best value is
+    shared by 70 or by 300 tokens: the 64th slice maximum F is tied, so the extraction gathers
+    every element that reaches F (70: within its buffer; 300: more than it holds, so every slice
+    is ranked); the kept ties are the lowest ids.  bf16, V = 50000."""
+    g = torch.Generator().manual_seed(64)
+    rows_per, V = 3, 50000
+    z = torch.randn(4 * rows_per, V, generator=g) * 2
+    for r in range(z.shape[0]):
+        n_tie = 300 if (r // rows_per) % 2 == 0 else 70
+        pos = torch.randperm(V, generator=g)[:n_tie]
+        z[r, pos] = z[r].max() + 1.0
+    z = z.bfloat16()
+    p = synth.make_params(4, [1.0, 1.0, 1.0, 1.0], [64, 64, 0, 0], [1.0, 1.0, 0.9, 0.5])
+    wide_compare(ref, z, p, rows_per, "ties at F")
+
+
 def test_wide_full_size(ref):
     """The 27B drafter's rows (448 x 151936 bf16) with top_p 0.95 and top_k off: every row."""
     dev = cuda_or_skip()
