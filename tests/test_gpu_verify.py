@@ -128,10 +128,12 @@ def test_wide_target_rows(ref, seed, dtype):
     assert 0 < int(np.sum(acc)) < B * K      # both accepts and rejects were exercised
 
 
-@pytest.mark.parametrize("k,p", [(20, 0.95), (0, 0.9)])
+@pytest.mark.parametrize("k,p", [(20, 0.95), (0, 0.9), (0, 1.0), (100, 1.0)])
 def test_gpu_monte_carlo_marginals(ref, k, p):
     """6M verify rows on the GPU: committed-token marginals within 5e-3 of p_t (top_k 20 with top_p
-    0.95, the pages' setting; and top_p 0.9 with top_k off, whose residual draws walk the whole row)."""
+    0.95, the pages' setting; then three targets whose p reaches past the 64 best, so that the
+    residual and bonus draws walk the whole row: top_p 0.9 with top_k off, no filter at all, and
+    top_k 100)."""
     dev = cuda_or_skip()
     B0, K, V = 4, 3, 2048
     shp = synth.small_shape("27b_sampled", B=B0, K=K, V=V, hidden=64, seed=31, target_noise=1.0)
