@@ -112,11 +112,12 @@ typedef struct {
  * parameters, gets cand_idx -1, U NaN and lse NaN.  Every filter is
  * supported: a row whose kept prefix reaches past its 64 best tokens (top_k
  * above 64, or top_p with top_k off) is finished with further passes over
- * the row (a radix select of the cut by count and by mass) by a second
- * kernel, which every call with params launches after the scan.
+ * the row (a radix select of the cut by count and by mass), in the same
+ * kernel: the CTA that completes such a row finishes it once it has
+ * streamed its share of the rows.
  * ws: dflash2_topk16_workspace_bytes(rows) bytes (the kernel splits long rows
- *   over several CTAs and combines the parts there, and lists the rows left
- *   to the second kernel).
+ *   over several CTAs and combines the parts there, and marks there the rows
+ *   a CTA finishes after its stream).
  * Errors: INVALID_ARG if a pointer is NULL or misaligned, rows < 0, V < 16,
  * V >= 2^31, ld < V, ld * elem size not a multiple of 16, rows_per_param < 1;
  * WORKSPACE if ws_bytes is too small.
@@ -134,9 +135,9 @@ dflash2_status dflash2_topk16(const void *logits, dflash2_dtype dt, int64_t rows
  * library device memory: a plugin, or an engine whose memory pool owns all
  * device memory and hands no scratch to the code it calls, or code that may
  * not call an allocator at the point where the drafter's rows are reduced.
- * The scratch (one ticket per row, the partial records of rows that the
- * kernel splits over several CTAs, the list of rows left to the second
- * kernel) is a fixed array in the library's own device memory, sized for
+ * The scratch (one ticket and one mark per row, and the partial records of
+ * rows that the kernel splits over several CTAs) is a fixed array in the
+ * library's own device memory, sized for
  * DFLASH2_TOPK16_NOALLOC_MAX_ROWS rows (about 1.2 MB),
  * held by every GPU that loads the library until the process exits.
  *   - rows > DFLASH2_TOPK16_NOALLOC_MAX_ROWS returns DFLASH2_ERR_WORKSPACE and
@@ -300,7 +301,8 @@ dflash2_status dflash2_pair_score_walk(int64_t B, int32_t K, const int32_t *cand
  *   p's support reaches past the row's 64 best tokens (no filter, top_p with
  *   top_k off, top_k above 64), the cut is found by further passes over the
  *   row and the residual and bonus draws walk the whole row in token-id order,
- *   in a second kernel that every call with params launches after the scan.
+ *   in the same kernel, by the CTA that completes the row once it has
+ *   streamed its share of the rows.
  * Outputs: accept_len [B] in 0..K; out_tok [B, K+1]: the accepted tokens,
  *   then the corrected or bonus token, then -1; status [B] (DFLASH2_ST_*).
  *   A request with status != 0 commits nothing (accept_len 0, all -1).
