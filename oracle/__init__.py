@@ -62,6 +62,7 @@ def lib():
             L.dflash2_ref_walk_accept_mc.argtypes = [i64, i64, i32, vp, vp, vp, vp, vp, vp, i64, vp, vp,
                                                      vp, vp, vp]
             L.dflash2_ref_conv2tap.argtypes = [vp, vp, vp, vp, i32, i64, i32, i64, i32, vp]
+            L.dflash2_ref_dynconv2tap.argtypes = [vp, vp, vp, i32, i64, i32, i64, i32, vp, vp]
             L.dflash2_ref_num_threads.restype = i32
             L.dflash2_ref_set_num_threads.argtypes = [i32]
             _lib = L
@@ -320,3 +321,19 @@ def conv2tap(x, k0, k1, x_prev, group=1):
         import torch
         return torch.from_numpy(y.view(np.int16)).view(torch.bfloat16)
     return y
+
+
+def dynconv2tap(x, x_prev, Wd, group=1):
+    """Grouped dynamic taps k0 = sigmoid(Wd . x_t) per group (k1 = 1 - k0) and the two-tap conv.
+    Returns (taps [B, T, H/group] float64, y with x's dtype)."""
+    xr, dt = _raw(x)
+    xpr, _ = _raw(x_prev)
+    wr, _ = _raw(Wd)
+    B, T, H = xr.shape
+    taps = np.empty((B, T, H // group), np.float64)
+    y = np.empty_like(xr)
+    lib().dflash2_ref_dynconv2tap(_p(xr), _p(xpr), _p(wr), dt, B, T, H, group, _p(taps), _p(y))
+    if dt == 1:
+        import torch
+        return taps, torch.from_numpy(y.view(np.int16)).view(torch.bfloat16)
+    return taps, y

@@ -985,6 +985,51 @@ void dflash2_ref_conv2tap(const void *x, const void *k0, const void *k1, const v
     }
 }
 
+/*
+ * Grouped dynamic taps.  The pages give the conv's form, "dynamic", and the
+ * group size (conv_group_size divides the hidden size), not how the taps are
+ * made; the reading here is dynamic convolution as published (Wu et al.,
+ * "Pay Less Attention with Lightweight and Dynamic Convolutions", 2019):
+ * position t's taps are a linear map of its own input, normalised by a
+ * softmax over the kernel's width and shared by the G channels of a group.
+ * With two taps, softmax(a0, a1) = (s, 1 - s) with s = sigmoid(a0 - a1), so
+ * the map enters through its difference Wd = W0 - W1, [H/G, H]:
+ *   k_{t,0}[g] = sigmoid(Wd[g] . x_t),  k_{t,1}[g] = 1 - k_{t,0}[g],
+ *   y_t[c] = k_{t,0}[c / G] x_t[c] + k_{t,1}[c / G] x_{t-1}[c]
+ * (x_prev at t = 0).  taps receives k_{t,0} in fp64, [B, T, H/G]; y is the
+ * fp64 value rounded once to the I/O dtype (nearest, ties to even).
+ */
+void dflash2_ref_dynconv2tap(const void *x, const void *x_prev, const void *Wd, int dtype, int64_t B, int T,
+                             int64_t H, int G, double *taps, void *y) {
+    int64_t Hk = H / G;
+#pragma omp parallel for collapse(2) schedule(static)
+    for (int64_t b = 0; b < B; b++) {
+        for (int t = 0; t < T; t++) {
+            int64_t row = b * T + t;
+            for (int64_t g = 0; g < Hk; g++) {
+                double a = 0.0;
+                for (int64_t c = 0; c < H; c++) a += ref_load(Wd, dtype, g * H + c) * ref_load(x, dtype, row * H + c);
+                taps[row * Hk + g] = 1.0 / (1.0 + exp(-a));
+            }
+            for (int64_t c = 0; c < H; c++) {
+                int64_t o = row * H + c;
+                double k0 = taps[row * Hk + c / G], k1 = 1.0 - k0;
+                double xc = ref_load(x, dtype, o);
+                double xp = t == 0 ? ref_load(x_prev, dtype, b * H + c) : ref_load(x, dtype, o - H);
+                double v = k0 * xc + k1 * xp;
+                if (dtype == REF_BF16) {
+                    float f = (float)round_bf16(v);
+                    uint32_t u;
+                    memcpy(&u, &f, 4);
+                    ((uint16_t *)y)[o] = (uint16_t)(u >> 16);
+                } else {
+                    ((float *)y)[o] = (float)v;
+                }
+            }
+        }
+    }
+}
+
 int dflash2_ref_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
