@@ -315,7 +315,7 @@ def run_ours(args, rank, world, local):
     # ---- the other workloads (sampled; stress) and the drafter-side conv, each with its own roofline ----
     aux = None
     if not args.no_kernel_pass:
-        aux = {"conv2tap": time_conv(dev, peak)}
+        aux = {"conv2tap": time_conv(dev, peak), "dynconv2tap": time_dynconv(dev, peak)}
         for name in AUX_WORKLOADS:
             if name != args.config:
                 aux[name] = time_workload(name, dev, peak, peak_kind)
@@ -488,6 +488,38 @@ def time_conv(dev, peak, reps=50):
     return {"workload": "stress conv [256, 16, 5120] bf16", "avg_launch_us": round(us, 2),
             "algorithmic_bytes": algo, "achieved": round(gbs, 1), "unit": "GB/s", "peak": peak,
             "frac": round(gbs / peak, 4), "bound": "hbm"}
+
+
+def time_dynconv(dev, peak, reps=50):
+    """dflash2_dynconv2tap at the stress workload's conv shape ([256, 16, 5120] bf16, group size 80:
+    64 groups): the taps' projection on the tensor cores, then the conv; mean of `reps` calls with
+    CUDA events.  Algorithmic bytes: x and x_prev read once, Wd, the taps and y written."""
+    import torch
+
+    import dflash_draft_selection_gb300 as d2
+    from dflash_draft_selection_gb300 import synth
+    shp = synth.WORKLOADS["stress"]
+    B, T, H, gs = shp.B, shp.K + 1, shp.hidden, 80
+    g = torch.Generator(device=dev).manual_seed(shp.seed + 1)
+    x = torch.randn(B, T, H, generator=g, device=dev).to(shp.dtype)
+    xp = torch.randn(B, H, generator=g, device=dev).to(shp.dtype)
+    W = (torch.randn(H // gs, H, generator=g, device=dev) * (2.0 / H ** 0.5)).to(shp.dtype)
+    out = (torch.empty(B, T, H // gs, dtype=torch.float32, device=dev), torch.empty_like(x))
+    for _ in range(3):
+        d2.dynconv2tap(x, xp, W, gs, out=out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        d2.dynconv2tap(x, xp, W, gs, out=out)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    algo = (2 * x.numel() + xp.numel() + W.numel()) * 2 + out[0].numel() * 4
+    gbs = algo / (us * 1e-6) / 1e9
+    return {"workload": f"stress dynamic conv [{B}, {T}, {H}] bf16, group size {gs}", "avg_launch_us": round(us, 2),
+            "algorithmic_bytes": algo, "achieved": round(gbs, 1), "unit": "GB/s", "peak": peak,
+            "frac": round(gbs / peak, 4), "bound": "hbm", "launches_per_call": 2}
 
 
 def run_e2e(chain, shp, dev, stream, steps, world):

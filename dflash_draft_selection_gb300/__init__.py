@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     conv2tap,
     ctx_gate,
     device_error,
+    dynconv2tap,
     lmhead_topk16,
     load_library,
     pair_score_walk,

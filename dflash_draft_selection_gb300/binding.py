@@ -64,6 +64,7 @@ def load_library():
         L.dflash2_verify.argtypes = [vp, i32, i64, i32, i64, i64, vp, vp, vp, vp, vp, vp, vp, u32, vp, vp, vp,
                                      vp, sz, vp]
         L.dflash2_conv2tap.argtypes = [vp, vp, vp, vp, i32, i64, i32, i64, i32, vp, vp]
+        L.dflash2_dynconv2tap.argtypes = [vp, vp, vp, i32, i64, i32, i64, i32, vp, vp, vp]
         L.dflash2_status_string.argtypes = [i32]
         L.dflash2_status_string.restype = ctypes.c_char_p
         L.dflash2_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
@@ -71,7 +72,8 @@ def load_library():
         for fn in ("dflash2_topk16", "dflash2_topk16_noalloc", "dflash2_topk16_shard", "dflash2_topk16_merge",
                    "dflash2_lmhead_topk16",
                    "dflash2_ctx_gate", "dflash2_pair_score_walk",
-                   "dflash2_verify", "dflash2_conv2tap", "dflash2_device_error", "dflash2_test_hold"):
+                   "dflash2_verify", "dflash2_conv2tap", "dflash2_dynconv2tap", "dflash2_device_error",
+                   "dflash2_test_hold"):
             getattr(L, fn).restype = i32
         _lib = L
         return _lib
@@ -335,6 +337,20 @@ def conv2tap(x, k0, k1, x_prev, group: int = 1, out=None):
     _check("dflash2_conv2tap", L.dflash2_conv2tap(_ptr(x), _ptr(k0), _ptr(k1), _ptr(x_prev), _dtype(x), B, T, H,
                                                   group, _ptr(y), _stream(x.device)))
     return y
+
+
+def dynconv2tap(x, x_prev, Wd, group: int = 1, out=None):
+    """dflash2_dynconv2tap.  x [B, T, H], x_prev [B, H], Wd [H/group, H].  Returns (taps [B, T, H/group]
+    f32, y [B, T, H])."""
+    L = load_library()
+    _need_cuda(x, x_prev, Wd)
+    B, T, H = x.shape
+    if out is None:
+        out = (torch.empty(B, T, H // group, dtype=torch.float32, device=x.device), torch.empty_like(x))
+    taps, y = out
+    _check("dflash2_dynconv2tap", L.dflash2_dynconv2tap(_ptr(x), _ptr(x_prev), _ptr(Wd), _dtype(x), B, T, H, group,
+                                                        _ptr(taps), _ptr(y), _stream(x.device)))
+    return taps, y
 
 
 def device_error(clear: bool = False) -> int:

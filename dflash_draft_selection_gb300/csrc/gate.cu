@@ -275,17 +275,16 @@ unsigned int read_error_gate(bool clear) {
 
 using namespace dfl;
 
-extern "C" dflash2_status dflash2_ctx_gate(const void *h, dflash2_dtype dt, int64_t n, int64_t hidden,
-                                           const void *Wg, int32_t D, float *gate, dflash2_stream stream) {
-    if (!dtype_ok(dt) || n < 0 || hidden < 1 || D < 16 || D > 512 || (D & (D - 1)) != 0)
-        return DFLASH2_ERR_INVALID_ARG;
-    if (dt == DFLASH2_BF16 && hidden % GBK != 0) return DFLASH2_ERR_INVALID_ARG;
-    if (n == 0) return DFLASH2_OK;
-    if (!h || !Wg || !gate || !aligned16(h) || !aligned16(Wg) || !aligned16(gate)) return DFLASH2_ERR_INVALID_ARG;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+namespace dfl {
+
+// gate = sigmoid(h . Wg^T) for checked arguments: bf16 on the tensor cores (D a
+// power of two in 16..512, hidden a multiple of 64), f32 on the CUDA cores (any D).
+dflash2_status gate_launch(const void *h, dflash2_dtype dt, int64_t n, int64_t hidden, const void *Wg, int D,
+                           float *gate, cudaStream_t s) {
     if (dt == DFLASH2_F32) {
         const int64_t warps = n * D;
         const int64_t blocks = (warps * 32 + 255) / 256;
+        if (blocks > 0x7fffffff) return DFLASH2_ERR_UNSUPPORTED;
         k_gate_f32<<<static_cast<unsigned>(blocks), 256, 0, s>>>(static_cast<const float *>(h),
                                                                  static_cast<const float *>(Wg), gate, n, hidden, D);
         return after_launch();
@@ -294,4 +293,16 @@ extern "C" dflash2_status dflash2_ctx_gate(const void *h, dflash2_dtype dt, int6
     if (D == 16) return launch_gate_tc<16>(h, n, hidden, Wg, D, gate, s);
     if (D == 32) return launch_gate_tc<32>(h, n, hidden, Wg, D, gate, s);
     return launch_gate_tc<64>(h, n, hidden, Wg, D, gate, s);
+}
+
+}  // namespace dfl
+
+extern "C" dflash2_status dflash2_ctx_gate(const void *h, dflash2_dtype dt, int64_t n, int64_t hidden,
+                                           const void *Wg, int32_t D, float *gate, dflash2_stream stream) {
+    if (!dtype_ok(dt) || n < 0 || hidden < 1 || D < 16 || D > 512 || (D & (D - 1)) != 0)
+        return DFLASH2_ERR_INVALID_ARG;
+    if (dt == DFLASH2_BF16 && hidden % GBK != 0) return DFLASH2_ERR_INVALID_ARG;
+    if (n == 0) return DFLASH2_OK;
+    if (!h || !Wg || !gate || !aligned16(h) || !aligned16(Wg) || !aligned16(gate)) return DFLASH2_ERR_INVALID_ARG;
+    return gate_launch(h, dt, n, hidden, Wg, D, gate, reinterpret_cast<cudaStream_t>(stream));
 }

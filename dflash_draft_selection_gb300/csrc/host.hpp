@@ -81,4 +81,9 @@ dflash2_status launch_merge16(int S, int64_t rows, const int32_t *part_idx, cons
                               int64_t rows_per_param, int32_t *cand_idx, float *cand_U, float *lse,
                               cudaStream_t stream);
 
+// gate = sigmoid(h . Wg^T) for checked arguments (gate.cu); the dynamic
+// convolution's taps.
+dflash2_status gate_launch(const void *h, dflash2_dtype dt, int64_t n, int64_t hidden, const void *Wg, int D,
+                           float *gate, cudaStream_t s);
+
 }  // namespace dfl

@@ -336,6 +336,35 @@ dflash2_status dflash2_conv2tap(const void *x, const void *k0, const void *k1, c
                                 dflash2_dtype dt, int64_t B, int32_t T, int64_t H,
                                 int32_t group_size, void *y, dflash2_stream stream);
 
+/*
+ * dflash2_dynconv2tap -- [P] item 2 with the taps made from the input: the
+ * pages name the conv "dynamic" and give its group size ([F] Refused at
+ * startup: conv_group_size divides the hidden size), not how the taps are
+ * made.  The reading is dynamic convolution as published (Wu et al., "Pay
+ * Less Attention with Lightweight and Dynamic Convolutions", 2019): the
+ * taps of position t are a linear map of x_t, normalised by a softmax over
+ * the kernel's width and shared by the group_size channels of a group.  For
+ * two taps that softmax is (s, 1 - s) with s = sigmoid(a0 - a1), so the map
+ * enters through its difference Wd:
+ *   taps[b, t, g] = k0 = sigmoid(Wd[g] . x[b, t]),  k1 = 1 - k0,
+ *   y[b, t, c] = k0 x[b, t, c] + k1 x[b, t-1, c]   (x_prev at t = 0, g = c / group_size).
+ *
+ * x [B, T, H], x_prev [B, H], Wd [H / group_size, H], y [B, T, H], all of dt;
+ * taps [B, T, H / group_size] f32 (an output).  bf16: the taps on the tensor
+ * cores (fp32 accumulation) as dflash2_ctx_gate computes its gate; y is
+ * fma(k0, x_t, k1 x_{t-1}) in fp32 rounded once to bf16 (within one bf16 ulp
+ * of the exact value).  f32: CUDA cores, y by one fused multiply-add.
+ * Not built: fusing the conv with the drafter sublayer's norm and residual
+ * (the pages give no form for them).
+ * Errors: INVALID_ARG for NULL/misaligned pointers (x, Wd, taps 16-byte
+ * aligned), B < 0, T < 1, H < 1, group_size < 1 or not dividing H;
+ * UNSUPPORTED for bf16 unless H is a multiple of 64 and H / group_size a
+ * power of two in 16..512.
+ */
+dflash2_status dflash2_dynconv2tap(const void *x, const void *x_prev, const void *Wd, dflash2_dtype dt,
+                                   int64_t B, int32_t T, int64_t H, int32_t group_size, float *taps, void *y,
+                                   dflash2_stream stream);
+
 /* Human-readable name of a status code (static string). */
 const char *dflash2_status_string(dflash2_status s);
 
