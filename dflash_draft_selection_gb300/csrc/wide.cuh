@@ -36,7 +36,6 @@ struct Team {
     int size;  // threads
     __device__ __forceinline__ void sync() const { __syncthreads(); }
     __device__ __forceinline__ int warp() const { return rank >> 5; }
-    __device__ __forceinline__ int warps() const { return size >> 5; }
 };
 
 // Histogram of a pass: counts and 64-bit fixed-point masses (two 32-bit
