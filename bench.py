@@ -34,11 +34,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "draft blocks/sec (topk+select+verify) at B=64,V=151936; % of HBM roofline"
 UNIT = "blocks/s"
-KERNEL_SOURCES = {
-    "k_topk16": ["common.cuh", "rowscan.cuh", "filter.cuh", "topk16.cu"],
-    "k_verify": ["common.cuh", "rowscan.cuh", "filter.cuh", "verify.cu"],
-    "k_gate_tc": ["common.cuh", "gate.cu"],
-    "k_pair_score_walk": ["common.cuh", "walk.cu"],
+KERNEL_SOURCES = {  # every file of the library each kernel is compiled from
+    "k_topk16": ["common.cuh", "host.hpp", "rowscan.cuh", "filter.cuh", "wide.cuh", "topk16.cu"],
+    "k_verify": ["common.cuh", "host.hpp", "rowscan.cuh", "filter.cuh", "wide.cuh", "verify.cu"],
+    "k_gate_tc": ["common.cuh", "host.hpp", "tc.cuh", "gate.cu"],
+    "k_pair_score_walk": ["common.cuh", "host.hpp", "walk.cu"],
 }
 
 
