@@ -181,6 +181,26 @@ def test_exactly_64_with_ties_at_f(ref):
     wide_compare(ref, z, p, rows_per, "ties at F")
 
 
+def test_many_wide_rows_per_cta(ref):
+    """16384 flat rows of V = 4096 with top_p 0.9 and top_k off: about 36 wide rows per CTA, every
+    one finished in its CTA's epilogue after the stream; 256 sampled rows against the oracle."""
+    dev = cuda_or_skip()
+    rows, V = 16384, 4096
+    g = torch.Generator(device=dev).manual_seed(36)
+    z = (torch.randn(rows, V, generator=g, device=dev) * 1.5).bfloat16()
+    p = synth.make_params(rows, 1.0, 0, 0.9)
+    pg = d2.sampling_params(p["temperature"], p["top_k"], p["top_p"], device=dev)
+    idx, U, lse = (t.cpu().numpy() for t in d2.topk16(z, params=pg))
+    assert d2.device_error() == 0
+    pick = np.random.default_rng(5).choice(rows, 256, replace=False)
+    zc = z[torch.as_tensor(pick, device=dev)].cpu()
+    r_idx, r_U, r_lse, _ = ref.topk16(zc, params=p[pick])
+    np.testing.assert_array_equal(idx[pick], r_idx)
+    assert np.all(np.isfinite(r_U))          # every cut is deeper than the 16 candidates
+    assert_close(U[pick], r_U, what="many wide rows U")
+    assert_close(lse[pick], r_lse, what="many wide rows lse")
+
+
 def test_wide_full_size(ref):
     """The 27B drafter's rows (448 x 151936 bf16) with top_p 0.95 and top_k off: every row."""
     dev = cuda_or_skip()

@@ -57,6 +57,21 @@ def test_noalloc_topk16_at_its_largest_batch():
     _same(got, ref, f"rows={MAX_ROWS}")
 
 
+def test_noalloc_topk16_wide_rows_at_its_largest_batch():
+    """top_p with top_k off on every row of the largest batch: each CTA marks and finishes about 36
+    wide rows in the fixed scratch; equal to the workspace call, twice in a row (the marks must
+    be cleared between calls)."""
+    dev = cuda_or_skip()
+    z = _logits(4, MAX_ROWS, 4096, dev)
+    p = d2.sampling_params([1.0], [0], [0.9], device=dev)
+    for _ in range(2):
+        got = d2.topk16_noalloc(z, params=p, rows_per_param=MAX_ROWS)
+        ref = d2.topk16(z, params=p, rows_per_param=MAX_ROWS)
+        torch.cuda.synchronize()
+        _same(got, ref, "wide rows")
+    assert d2.device_error() == 0
+
+
 def test_noalloc_topk16_rejects_batches_beyond_its_array():
     cuda_or_skip()
     L = d2.load_library()
