@@ -202,7 +202,8 @@ extern "C" dflash2_status dflash2_dynconv2tap(const void *x, const void *x_prev,
     if (dt == DFLASH2_BF16 && (H % 64 != 0 || Hk < 16 || Hk > 512 || (Hk & (Hk - 1)) != 0))
         return DFLASH2_ERR_UNSUPPORTED;  // the tensor-core taps' tiles
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const dflash2_status st = gate_launch(x, dt, B * T, H, Wd, static_cast<int>(Hk), taps, s);
+    // x is typically the previous kernel's output: the projection starts after it completes
+    const dflash2_status st = gate_launch(x, dt, B * T, H, Wd, static_cast<int>(Hk), taps, s, false);
     if (st != DFLASH2_OK) return st;
     DynArgs a{x, x_prev, taps, y, B, H, T, group_size};
     const bool vec = dt == DFLASH2_BF16 && H % 8 == 0 && group_size % 8 == 0 && aligned16(x_prev) && aligned16(y);

@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(256) k_gate_f32(const float *h, const float *W
 // ------------------------------------------------------------------ host ----
 template <int BN>
 static dflash2_status launch_gate_tc(const void *h, int64_t n, int64_t hidden, const void *Wg, int D, float *gate,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, bool early) {
     CUtensorMap tm_h, tm_w;
     if (!make_map_k64(&tm_h, h, static_cast<uint64_t>(hidden), static_cast<uint64_t>(n), GBM) ||
         !make_map_k64(&tm_w, Wg, static_cast<uint64_t>(hidden), static_cast<uint64_t>(D), BN))
@@ -255,7 +255,7 @@ static dflash2_status launch_gate_tc(const void *h, int64_t n, int64_t hidden, c
     attr[0].val.clusterDim.z = static_cast<unsigned>(ks);
     attr[1] = pdl_attribute();
     cfg.attrs = attr;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = early ? 2 : 1;  // without it the grid starts after the previous one completes
     if (cudaLaunchKernelEx(&cfg, k_gate_tc<BN>, tm_h, tm_w, gate, n, D, kblocks, ks) != cudaSuccess)
         return DFLASH2_ERR_CUDA;
     return after_launch();
@@ -279,8 +279,10 @@ namespace dfl {
 
 // gate = sigmoid(h . Wg^T) for checked arguments: bf16 on the tensor cores (D a
 // power of two in 16..512, hidden a multiple of 64), f32 on the CUDA cores (any D).
+// With `early` the tensor-core grid may start while the previous grid runs
+// (programmatic dependent launch): h and Wg must not be written by it.
 dflash2_status gate_launch(const void *h, dflash2_dtype dt, int64_t n, int64_t hidden, const void *Wg, int D,
-                           float *gate, cudaStream_t s) {
+                           float *gate, cudaStream_t s, bool early) {
     if (dt == DFLASH2_F32) {
         const int64_t warps = n * D;
         const int64_t blocks = (warps * 32 + 255) / 256;
@@ -290,9 +292,9 @@ dflash2_status gate_launch(const void *h, dflash2_dtype dt, int64_t n, int64_t h
         return after_launch();
     }
     if (n >= (int64_t(1) << 31)) return DFLASH2_ERR_UNSUPPORTED;
-    if (D == 16) return launch_gate_tc<16>(h, n, hidden, Wg, D, gate, s);
-    if (D == 32) return launch_gate_tc<32>(h, n, hidden, Wg, D, gate, s);
-    return launch_gate_tc<64>(h, n, hidden, Wg, D, gate, s);
+    if (D == 16) return launch_gate_tc<16>(h, n, hidden, Wg, D, gate, s, early);
+    if (D == 32) return launch_gate_tc<32>(h, n, hidden, Wg, D, gate, s, early);
+    return launch_gate_tc<64>(h, n, hidden, Wg, D, gate, s, early);
 }
 
 }  // namespace dfl
@@ -304,5 +306,5 @@ extern "C" dflash2_status dflash2_ctx_gate(const void *h, dflash2_dtype dt, int6
     if (dt == DFLASH2_BF16 && hidden % GBK != 0) return DFLASH2_ERR_INVALID_ARG;
     if (n == 0) return DFLASH2_OK;
     if (!h || !Wg || !gate || !aligned16(h) || !aligned16(Wg) || !aligned16(gate)) return DFLASH2_ERR_INVALID_ARG;
-    return gate_launch(h, dt, n, hidden, Wg, D, gate, reinterpret_cast<cudaStream_t>(stream));
+    return gate_launch(h, dt, n, hidden, Wg, D, gate, reinterpret_cast<cudaStream_t>(stream), true);
 }

@@ -82,8 +82,8 @@ dflash2_status launch_merge16(int S, int64_t rows, const int32_t *part_idx, cons
                               cudaStream_t stream);
 
 // gate = sigmoid(h . Wg^T) for checked arguments (gate.cu); the dynamic
-// convolution's taps.
+// convolution's taps.  `early`: the grid may start beside the previous one.
 dflash2_status gate_launch(const void *h, dflash2_dtype dt, int64_t n, int64_t hidden, const void *Wg, int D,
-                           float *gate, cudaStream_t s);
+                           float *gate, cudaStream_t s, bool early);
 
 }  // namespace dfl

@@ -234,6 +234,11 @@ dflash2_status dflash2_lmhead_topk16(const void *h, const void *W, int64_t rows,
  *
  * h     [n, hidden] of dt;  Wg [D, hidden] of dt;  gate [n, D] f32.
  * bf16 runs on the tensor cores (fp32 accumulation); f32 on the CUDA cores.
+ * The bf16 grid may start while the previous kernel in the stream still
+ * runs, once that kernel allows it (programmatic dependent launch; of this
+ * library's kernels, the row scans allow it at their start), so that it
+ * overlaps dflash2_topk16's tail: h and Wg must not be written by the
+ * kernel just before it.  It completes only after that kernel does.
  * Errors: INVALID_ARG if a pointer is NULL or misaligned, n < 0, D not in
  * {16, 32, ..., 512} (a power of two), hidden < 1, or (bf16) hidden not a
  * multiple of 64.
