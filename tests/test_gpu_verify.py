@@ -128,6 +128,20 @@ def test_wide_target_rows(ref, seed, dtype):
     assert 0 < int(np.sum(acc)) < B * K      # both accepts and rejects were exercised
 
 
+def test_wide_and_narrow_requests_in_one_call(ref):
+    """One batch mixing greedy requests, top_k 20 with top_p 0.95 (p within the 64 best), and
+    wide targets (top_p 0.9 with top_k off, top_k 100): wide rows finished in their CTAs'
+    epilogues next to rows finished at completion, against the oracle."""
+    B, K, V = 16, 5, 20000
+    shp = synth.small_shape("27b_sampled", B=B, K=K, V=V, hidden=64, seed=9, target_noise=1.0)
+    inp = synth.make_inputs(shp, with_conv=False)
+    inp.params["temperature"] = np.resize(np.float32([0.0, 1.0, 1.0, 0.9]), B)
+    inp.params["top_k"] = np.resize(np.int32([0, 20, 0, 100]), B)
+    inp.params["top_p"] = np.resize(np.float32([1.0, 0.95, 0.9, 1.0]), B)
+    cand, pt, ps, q = oracle_walk_inputs(ref, inp, B, K)
+    check(ref, inp, cand, pt, ps, q, inp.params, B, K)
+
+
 @pytest.mark.parametrize("k,p", [(20, 0.95), (0, 0.9), (0, 1.0), (100, 1.0)])
 def test_gpu_monte_carlo_marginals(ref, k, p):
     """6M verify rows on the GPU: committed-token marginals within 5e-3 of p_t (top_k 20 with top_p
